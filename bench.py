@@ -1,0 +1,444 @@
+"""Benchmark of the Gated DeltaNet recurrence on GB300.
+
+One step = one gdn_prefill call on the 4096-token prompt workload
+(B=1, T=4096, 16 key / 32 value heads, d_k = d_v = 128, bf16 q/k/v, fp32 g,
+beta and state, zero initial state), inputs resident in HBM; L2 is flushed
+(a buffer of twice the L2 size is written) between timed steps.  The decode
+half of the headline metric is measured in the same run on the batched decode
+workload (256 sequences, one token each, state updated in place) and on the
+batch-1 decode through 30 layers (one CUDA graph of 30 calls per step).
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own replica
+(independent prompts; no collective on the data path) and the time is the max
+over ranks: weak scaling.
+
+--impl reference times the fp64 CPU oracle (the only reference this build
+has) on the host cores for the same workload and metric.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN tokens/s: prefill T=4K (tensor-pipe %) & decode state HBM GB/s (% peak)"
+WORKLOAD = "prefill_t4096"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+NUM_SMS_GB300 = 152
+FP32_LANES_PER_SM = 128
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(PEAKS_FALLBACK)
+    d["source"] = "fallback"
+    return d
+
+
+# ---------------------------------------------------------------- algorithmic work
+def prefill_bytes(T, N, h_k, h_v, d_k, d_v, esize, state_in):
+    qk = 2 * T * h_k * d_k * esize
+    vo = 2 * T * h_v * d_v * esize
+    gb = 2 * T * h_v * 4
+    st = N * h_v * d_v * d_k * 4 * (2 if state_in else 1)
+    return qk + vo + gb + st
+
+
+def chunked_flops_per_token(h_k, h_v, d_k, d_v, C=64):
+    """Dense MMA work the chunked form issues (2 flop per multiply-add):
+    per (chunk, key head) K K^T and Q K^T; per (chunk, value head) W, U~ and
+    P U (C x C x d products), W S^T, Q S^T and the state update (C x d_k x d_v),
+    and the triangular solve (C^3/3 multiply-adds)."""
+    per_key = 2 * (2 * C * C * d_k)
+    per_val = 2 * C * C * d_k + 2 * 2 * C * C * d_v + 3 * (2 * C * d_k * d_v) + 2 * C ** 3 // 3
+    return (h_k * per_key + h_v * per_val) / C
+
+
+def scan_flops_per_token(h_v, d_k, d_v):
+    """Row identity per (token, value head): s = S k, p = S q and the rank-1
+    update, 3 multiply-adds per state element."""
+    return 6 * d_k * d_v * h_v
+
+
+def decode_bytes(B, h_k, h_v, d_k, d_v, esize):
+    state = 2 * B * h_v * d_v * d_k * 4
+    return state + 2 * B * h_k * d_k * esize + 2 * B * h_v * d_v * esize + 2 * B * h_v * 4
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    import numpy as np
+    import oracle
+    from gated_deltanet_linear_recurrence_gb300 import inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[WORKLOAD]
+    d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                            seed=w["seed"])
+    T = sum(w["lengths"])
+    threads = oracle.default_threads()
+
+    def step():
+        oracle.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], w["h_k"],
+                       w["h_v"], w["d_k"], w["d_v"], state_in=None, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = time.perf_counter() - t0
+    value = args.steps * T / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} (B=1, T=4096, H_k=16, H_v=32, d_k=d_v=128, bf16 "
+                               "inputs widened to fp64, zero initial state)",
+                   "global_batch": 1, "seq_len": T, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": "the whole workload each step (all 32 heads, 4096 tokens)"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(d, w, budget_s=12.0):
+    """The oracle as it stands, on the host cores, over whole-workload passes
+    until about budget_s seconds have elapsed (at least one pass)."""
+    import oracle
+
+    threads = oracle.default_threads()
+    T = sum(w["lengths"])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], w["h_k"],
+                       w["h_v"], w["d_k"], w["d_v"], state_in=d["state_in"], threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 8:
+            break
+    sec = time.perf_counter() - t0
+    return {"value": reps * T / sec, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} pass(es) over the whole {WORKLOAD} workload ({sec:.1f} s)"}
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_linear_recurrence_gb300 import (_lib, gdn_decode_step, gdn_prefill,
+                                                        gdn_prefill_crossover_tokens,
+                                                        gdn_prefill_workspace_size,
+                                                        gdn_stream_status, inputs)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = _lib.load()
+    peaks = load_peaks()
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    h_k, h_v, d_k, d_v = w["h_k"], w["h_v"], w["d_k"], w["d_v"]
+    T = sum(w["lengths"])
+    d = inputs.make_prefill(w["lengths"], h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + rank)
+    x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    o = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((1, h_v, d_v, d_k), dtype=torch.float32, device=dev)
+    ws_n = gdn_prefill_workspace_size(1, T, h_k, h_v, d_k, d_v, torch.bfloat16, args.algo)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cross = gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, torch.bfloat16)
+    algo_used = args.algo if args.algo != "auto" else ("chunked" if T >= cross else "scan")
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def prefill_once():
+        gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], state_in=None,
+                    state_out=st, o=o, algo=args.algo, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush()
+        prefill_once()
+    torch.cuda.synchronize()
+    assert gdn_stream_status(stream) == "GDN_OK"
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush()
+        starts[i].record(stream)
+        prefill_once()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+    launches_per_step = 1
+
+    # roofline of the prefill kernel (one launch per step)
+    if algo_used == "chunked":
+        flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
+        achieved = flop / (ms_per_step / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                "algorithmic_flop_per_launch": flop}
+    else:
+        flop = scan_flops_per_token(h_v, d_k, d_v) * T
+        achieved = flop / (ms_per_step / 1e3) / 1e12
+        fp32_peak = NUM_SMS_GB300 * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp32_peak, "traffic": None,
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
+                "algorithmic_flop_per_launch": flop}
+    hbm_bytes = prefill_bytes(T, 1, h_k, h_v, d_k, d_v, 2, False)
+    roof["hbm_gbs_at_algorithmic_bytes"] = hbm_bytes / (ms_per_step / 1e3) / 1e9
+
+    # e2e: host buffers in, results out, through the same call
+    pin = {k: d[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    cu_host = d["cu_seqlens"].pin_memory()
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    st_host = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    bufs = {k: torch.empty_like(x[k]) for k in ("q", "k", "v", "g", "beta")}
+    cu_dev = torch.empty_like(x["cu_seqlens"])
+
+    def e2e_once():
+        for k in bufs:
+            bufs[k].copy_(pin[k], non_blocking=True)
+        cu_dev.copy_(cu_host, non_blocking=True)
+        gdn_prefill(bufs["q"], bufs["k"], bufs["v"], bufs["g"], bufs["beta"], cu_dev,
+                    state_in=None, state_out=st, o=o, algo=args.algo, workspace=ws,
+                    stream=stream)
+        o_host.copy_(o, non_blocking=True)
+        st_host.copy_(st, non_blocking=True)
+
+    for _ in range(3):
+        e2e_once()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(args.steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_once()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in pin) + cu_host.numel() * 4
+    d2h = o_host.numel() * 2 + st_host.numel() * 4
+    e2e = {"value": world * T / (statistics.mean(e_ms) / 1e3), "unit": "tok/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "path": "pinned host -> device copies, gdn_prefill, device -> host copies"}
+
+    # decode half of the metric
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush)
+
+    clk = clocks.stop()
+    assert gdn_stream_status(stream) == "GDN_OK"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} (B=1, T=4096, H_k=16, H_v=32, d_k=d_v=128, bf16 "
+                               "q/k/v, fp32 g/beta/state, zero initial state)",
+                   "global_batch": world, "seq_len": T,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "algo": algo_used, "l2": "flushed between timed steps (2x L2 buffer written)"},
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+        "decode": decode,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, w)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush):
+    out = {}
+    # batched decode: 256 sequences; 1 GiB of state, far above L2
+    w = inputs.WORKLOADS["decode_b256"]
+    dd = inputs.make_decode(w["batch"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                            seed=w["seed"])
+    y = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dd.items()}
+    o = torch.empty_like(y["v"])
+
+    def step():
+        gdn_decode_step(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"], o=o, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    nbytes = decode_bytes(w["batch"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], 2)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["decode_b256"] = {"us_per_step": ms * 1e3, "bytes_per_step": nbytes, "gbs": gbs,
+                          "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                          "frac_of_8tbs_nominal": gbs / 8000.0,
+                          "tok_s": w["batch"] / (ms / 1e3), "l2": "state 1 GiB > L2"}
+    out["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                       "peak_source": f"{peaks['source']} copy bandwidth"}
+    del y, o, dd
+
+    # batch-1 decode through 30 layers: one CUDA graph of 30 calls per step
+    w = inputs.WORKLOADS["decode_b1_x30layers"]
+    layers = []
+    for layer in range(w["layers"]):
+        dd = inputs.make_decode(1, w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                                seed=w["seed"] * 100 + layer)
+        layers.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+                       for k, v in dd.items()})
+    outs = [torch.empty_like(L["v"]) for L in layers]
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for L, ob in zip(layers, outs):  # warm the launch path outside capture
+            gdn_decode_step(L["q"], L["k"], L["v"], L["g"], L["beta"], L["state"], o=ob,
+                            stream=side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for L, ob in zip(layers, outs):
+            gdn_decode_step(L["q"], L["k"], L["v"], L["g"], L["beta"], L["state"], o=ob,
+                            stream=side)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ms_list = []
+    for _ in range(args.steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_list.append(a.elapsed_time(b))
+    ms = statistics.median(ms_list)
+    nbytes = w["layers"] * decode_bytes(1, w["h_k"], w["h_v"], w["d_k"], w["d_v"], 2)
+    out["decode_b1_x30layers"] = {"us_per_step": ms * 1e3, "us_per_layer": ms * 1e3 / 30,
+                                  "bytes_per_step": nbytes,
+                                  "gbs": nbytes / (ms / 1e3) / 1e9,
+                                  "tok_s": 1 / (ms / 1e3),
+                                  "l2": "flushed between steps; 30 calls in one CUDA graph"}
+    return out
+
+
+if __name__ == "__main__":
+    main()

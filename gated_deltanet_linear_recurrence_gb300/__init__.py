@@ -1,1 +1,119 @@
-"""GB300-native Gated DeltaNet recurrence (placeholder until the binding lands)."""
+"""GB300-native (sm_103a) Gated DeltaNet recurrence.
+
+Python face of the C ABI in include/gdn.h.  The functions below carry the
+ABI's names; they take torch CUDA tensors (PyTorch supplies device memory and
+streams), marshal pointers and sizes, and call the CUDA library.  Outputs not
+passed in are allocated with torch.  Nothing here computes the recurrence.
+
+    S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t (scale q_t)
+"""
+import torch
+
+from . import _lib
+from ._lib import GdnError, STATUS_NAMES
+
+__all__ = ["gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_size", "gdn_stream_status",
+           "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError", "STATUS_NAMES"]
+
+_DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t):
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _require(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def gdn_status_string(status):
+    return _lib.load().gdn_status_string(int(status)).decode()
+
+
+def gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, dtype=torch.bfloat16):
+    return int(_lib.load().gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, _DTYPES[dtype]))
+
+
+def gdn_prefill_workspace_size(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype=torch.bfloat16,
+                               algo="auto"):
+    return int(_lib.load().gdn_prefill_workspace_size(num_seqs, total_tokens, h_k, h_v, d_k, d_v,
+                                                      _DTYPES[dtype], _lib.ALGOS[algo]))
+
+
+def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=None, scale=1.0,
+                algo="auto", workspace=None, stream=None):
+    """Prefill N packed sequences (see gdn_prefill in include/gdn.h).
+
+    q, k [T, h_k, d_k]; v [T, h_v, d_v] (fp32 or bf16); g, beta [T, h_v] fp32;
+    cu_seqlens [N+1] int32 on the device; state_in [N, h_v, d_v, d_k] fp32 or
+    None (zeros).  Returns (o [T, h_v, d_v], state_out [N, h_v, d_v, d_k]).
+    """
+    lib = _lib.load()
+    T, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    _require(k.shape == q.shape and v.shape[0] == T, "q/k/v shapes disagree")
+    _require(g.shape == (T, h_v) and beta.shape == (T, h_v), "g/beta must be [T, h_v]")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    _require(cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda, "cu_seqlens: int32 on GPU")
+    for t in (q, k, v, g, beta, cu_seqlens):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    _require(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share a dtype")
+    if o is None:
+        o = torch.empty((T, h_v, d_v), dtype=q.dtype, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((N, h_v, d_v, d_k), dtype=torch.float32, device=q.device)
+    if state_in is not None:
+        _require(state_in.dtype == torch.float32 and state_in.is_contiguous(), "state_in fp32")
+    need = lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt, _lib.ALGOS[algo])
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), N, T, h_k, h_v, d_k, d_v,
+                         dt, float(scale), _lib.ALGOS[algo], _ptr(workspace), ws_bytes,
+                         _stream(stream))
+    _lib.check(st, "gdn_prefill")
+    return o, state_out
+
+
+def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None):
+    """One token per sequence, state [B, h_v, d_v, d_k] fp32 updated in place.
+
+    q, k [B, h_k, d_k]; v [B, h_v, d_v]; g, beta [B, h_v] fp32.  Returns o [B, h_v, d_v].
+    """
+    lib = _lib.load()
+    B, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    _require(k.shape == q.shape and v.shape[0] == B, "q/k/v shapes disagree")
+    _require(state.shape == (B, h_v, d_v, d_k) and state.dtype == torch.float32,
+             "state must be [B, h_v, d_v, d_k] fp32")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    for t in (q, k, v, g, beta, state):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((B, h_v, d_v), dtype=q.dtype, device=q.device)
+    st = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                             _ptr(o), B, h_k, h_v, d_k, d_v, dt, float(scale), _stream(stream))
+    _lib.check(st, "gdn_decode_step")
+    return o
+
+
+def gdn_stream_status(stream=None):
+    """Synchronise the stream; return (and clear) the device error word as a status name."""
+    return STATUS_NAMES.get(int(_lib.load().gdn_stream_status(_stream(stream))), "unknown")

@@ -1,0 +1,138 @@
+// decode_step.cu — fused single-token update of the gated delta rule for a
+// batch of independent sequences, state updated in place.
+//
+// Page "Optimizing on-device inference for Apple Silicon", section "Reduce
+// intermediate and state traffic": the decode-time recurrent update runs as one
+// fused kernel whose temporaries stay in registers.  Section "Decode: minimize
+// bytes moved per token": decode throughput is set by the bytes moved, so the
+// kernel reads every state element once and writes it once (128-bit coalesced
+// accesses: a warp-wide load covers 512 contiguous bytes, as in the page's
+// "Coalesce attention-cache reads") and does all arithmetic on the way through.
+//
+// Work split.  One CTA of 4 warps owns a block of rows of one (sequence, value
+// head); each warp holds kRowsPerWarp rows (see rows.cuh) and issues all of its
+// state loads before any arithmetic so that many bytes are in flight per SM.
+// k and q are read once per warp, v once per row.  The state is HBM traffic
+// (1 GiB per step at 256 sequences x 32 heads x 128 x 128 fp32, read + write);
+// everything else is under 1% of the bytes.
+#include <cuda_bf16.h>
+
+#include "params.h"
+#include "rows.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kDecodeWarps = 4;
+
+template <int DK, int R, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                       const float* __restrict__ g, const float* __restrict__ beta,
+                       float* __restrict__ state, T* __restrict__ o, int32_t h_k, int32_t h_v,
+                       int32_t d_v, int32_t blocks_per_head, float scale) {
+  constexpr int L = DK / 4;  // one float4 per lane per row
+  using LY = RowLayout<DK, L, R>;
+  constexpr int M = LY::M;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int b = blockIdx.x / blocks_per_head;
+  const int rb = blockIdx.x - b * blocks_per_head;
+  const int h = blockIdx.y;
+  const int row0 = (rb * kDecodeWarps + warp) * LY::kRowsPerWarp;
+  if (row0 >= d_v) return;  // whole warp idle (d_v is a multiple of 16)
+  const int grp = lane / L;
+  const int lam = lane % L;
+  const int hk = h / (h_v / h_k);
+  const int64_t bh = (int64_t)b * h_v + h;
+
+  // state rows first: they are the bytes that matter
+  float* srow = state + (bh * d_v + row0 + grp) * (int64_t)DK + 4 * lam;
+  float4 s[R][M];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      s[r][m] = __ldcs(reinterpret_cast<const float4*>(srow + (int64_t)r * LY::G * DK + 4 * L * m));
+
+  const T* kp = k + ((int64_t)b * h_k + hk) * DK + 4 * lam;
+  const T* qp = q + ((int64_t)b * h_k + hk) * DK + 4 * lam;
+  float4 k4[M], q4[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    k4[m] = load4(kp + 4 * L * m);
+    q4[m] = load4(qp + 4 * L * m);
+    q4[m].x *= scale;
+    q4[m].y *= scale;
+    q4[m].z *= scale;
+    q4[m].w *= scale;
+  }
+  const int idx = lam / LY::Q;  // reduced value index this lane will hold
+  const int r_mine = idx >> 1;
+  const int row_mine = row0 + r_mine * LY::G + grp;
+  const float v_mine = load1(v + bh * d_v + row_mine);
+  const float alpha = expf(__ldg(g + bh));
+  const float bt = __ldg(beta + bh);
+
+  float kq = 0.f;
+#pragma unroll
+  for (int m = 0; m < M; ++m) kq = dot4(k4[m], q4[m], kq);
+  kq = group_sum<L>(kq);
+
+  const float out = row_token_update<DK, L, R>(s, k4, q4, kq, alpha, bt, v_mine, lane);
+  if ((idx & 1) && (lam % LY::Q) == 0) store1(o + bh * d_v + row_mine, out);
+
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      __stcs(reinterpret_cast<float4*>(srow + (int64_t)r * LY::G * DK + 4 * L * m), s[r][m]);
+}
+
+template <int DK, int R, typename T>
+cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int L = DK / 4;
+  constexpr int rows_per_block = kDecodeWarps * RowLayout<DK, L, R>::kRowsPerWarp;
+  const int blocks_per_head = (a.d_v + rows_per_block - 1) / rows_per_block;
+  const int64_t gx = (int64_t)a.batch * blocks_per_head;
+  if (gx > 0x7fffffffLL || a.h_v > 65535) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)gx, (unsigned)a.h_v);
+  decode_step_kernel<DK, R, T><<<grid, kDecodeWarps * 32, 0, stream>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
+      a.beta, a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale);
+  return cudaGetLastError();
+}
+
+// Rows per lane group: R = L/2 gives 16 rows per warp (most bytes in flight
+// per warp); with few rows in total a smaller R spreads the work over more SMs.
+template <int DK, typename T>
+cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int L = DK / 4;
+  constexpr int R_BIG = L / 2;
+  constexpr int R_SMALL = (L / 8) > 0 ? (L / 8) : 1;
+  const int64_t rows = (int64_t)a.batch * a.h_v * a.d_v;
+  // 16 rows per warp still gives >= 4 warps on every one of 152 SMs
+  if (rows >= (int64_t)16 * 4 * 152 * kDecodeWarps) return launch_t<DK, R_BIG, T>(a, stream);
+  return launch_t<DK, R_SMALL, T>(a, stream);
+}
+
+template <typename T>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.d_k) {
+    case 16: return launch_dk<16, T>(a, stream);
+    case 32: return launch_dk<32, T>(a, stream);
+    case 64: return launch_dk<64, T>(a, stream);
+    case 128: return launch_dk<128, T>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.batch == 0) return cudaSuccess;
+  if (a.dtype == kBF16) return launch_typed<__nv_bfloat16>(a, stream);
+  return launch_typed<float>(a, stream);
+}
+
+}  // namespace gdn

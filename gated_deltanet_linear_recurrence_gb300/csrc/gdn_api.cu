@@ -1,0 +1,194 @@
+// gdn_api.cu — the C ABI: argument validation, algorithm choice, launches,
+// and the per-device error word.  Declarations and contracts: include/gdn.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gdn.h"
+#include "params.h"
+
+namespace {
+
+// Device-side error word (one per device that loads the library).  Kernels
+// receive its address as an argument; gdn_stream_status reads and clears it.
+__device__ int g_gdn_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+gdn_status error_word(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gdn_error_word) != cudaSuccess) return GDN_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return GDN_OK;
+}
+
+bool head_dim_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
+  if (h_k <= 0 || h_v <= 0 || d_k <= 0 || d_v <= 0) return GDN_ERR_INVALID_ARG;
+  if (h_v % h_k != 0 || !head_dim_ok(d_k) || !head_dim_ok(d_v) || h_v > 65535)
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  return GDN_OK;
+}
+
+// Measured crossover (sequence length from which the chunked evaluation is
+// faster than the token scan) for bf16 inputs, by head dimension.
+int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
+  if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return INT32_MAX;
+  return 64;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL_POINTER: return "GDN_ERR_NULL_POINTER";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED_SHAPE: return "GDN_ERR_UNSUPPORTED_SHAPE";
+    case GDN_ERR_UNSUPPORTED_DTYPE: return "GDN_ERR_UNSUPPORTED_DTYPE";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_BAD_CU_SEQLENS: return "GDN_ERR_BAD_CU_SEQLENS";
+    case GDN_ERR_WORKSPACE_TOO_SMALL: return "GDN_ERR_WORKSPACE_TOO_SMALL";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+int32_t gdn_prefill_crossover_tokens(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v,
+                                     gdn_dtype dtype) {
+  if (check_heads(h_k, h_v, d_k, d_v) != GDN_OK) return INT32_MAX;
+  return crossover_for(h_k, h_v, d_k, d_v, dtype);
+}
+
+size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
+                                  int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                                  gdn_algo algo) {
+  if (num_seqs < 0 || total_tokens < 0 || check_heads(h_k, h_v, d_k, d_v) != GDN_OK) return 0;
+  if (algo == GDN_ALGO_SCAN) return 0;
+  if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return 0;
+  return gdn::chunked_workspace_bytes(num_seqs, total_tokens, h_k, h_v, d_k, d_v);
+}
+
+gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, const float* state_in, float* state_out, void* o,
+                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                       float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                       gdn_stream_t stream) {
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  if (st != GDN_OK) return st;
+  if (total_tokens > INT32_MAX) return GDN_ERR_UNSUPPORTED_SHAPE;  // cu_seqlens is int32
+  if (num_seqs == 0) return GDN_OK;
+  if (!cu_seqlens || !state_out) return GDN_ERR_NULL_POINTER;
+  if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_NULL_POINTER;
+  const void* ptrs[] = {q, k, v, g, beta, state_in, state_out, o, cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  // state_in may be state_out exactly; any partial overlap is refused
+  const size_t state_bytes = (size_t)num_seqs * h_v * d_v * d_k * sizeof(float);
+  if (state_in && state_in != state_out) {
+    const char* a = reinterpret_cast<const char*>(state_in);
+    const char* b = reinterpret_cast<const char*>(state_out);
+    if (a < b + state_bytes && b < a + state_bytes) return GDN_ERR_INVALID_ARG;
+  }
+  const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
+  if (algo == GDN_ALGO_CHUNKED && !chunk_ok)
+    return dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE;
+
+  gdn::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state_in = state_in; a.state_out = state_out; a.o = o; a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs; a.total_tokens = total_tokens;
+  a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
+  a.dtype = dtype; a.scale = scale;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+
+  // Which kernels run: scan for sequences shorter than min_chunk_len, chunked
+  // for the rest.  With one sequence its length is total_tokens, so the host
+  // can launch only the kernel that has work.
+  bool run_scan = true, run_chunk = false;
+  if (algo == GDN_ALGO_SCAN) {
+    a.min_chunk_len = INT32_MAX;
+  } else if (algo == GDN_ALGO_CHUNKED) {
+    a.min_chunk_len = 0;
+    run_scan = false;
+    run_chunk = true;
+  } else {
+    a.min_chunk_len = crossover_for(h_k, h_v, d_k, d_v, dtype);
+    run_chunk = chunk_ok && total_tokens >= a.min_chunk_len;
+    run_scan = !(num_seqs == 1 && run_chunk);
+  }
+  if (run_chunk) {
+    const size_t need = gdn::chunked_workspace_bytes(num_seqs, total_tokens, h_k, h_v, d_k, d_v);
+    if (workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !workspace) return GDN_ERR_NULL_POINTER;
+    if (workspace && !aligned16(workspace)) return GDN_ERR_MISALIGNED;
+  }
+  st = error_word(&a.err);
+  if (st != GDN_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (run_chunk && gdn::launch_chunked(a, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (run_scan && gdn::launch_scan(a, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, void* o, int32_t batch, int32_t h_k,
+                           int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
+                           gdn_stream_t stream) {
+  if (batch < 0) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  if (st != GDN_OK) return st;
+  if (batch == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !state || !o) return GDN_ERR_NULL_POINTER;
+  const void* ptrs[] = {q, k, v, g, beta, state, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+  gdn::DecodeArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.o = o;
+  a.batch = batch; a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
+  a.dtype = dtype; a.scale = scale;
+  if (gdn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+gdn_status gdn_stream_status(gdn_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  int* err = nullptr;
+  gdn_status st = error_word(&err);
+  if (st != GDN_OK) return st;
+  int word = 0;
+  if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
+  return static_cast<gdn_status>(word);
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// params.h — launch arguments passed from the C ABI layer to the kernels.
+// Plain structs of pointers and sizes; no torch types.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+enum Dtype : int { kF32 = 0, kBF16 = 1 };
+
+// Device error codes written to the library's error word (same values as
+// gdn_status in include/gdn.h).
+enum DeviceError : int { kErrBadCuSeqlens = 6, kErrDeviceTimeout = 8 };
+
+struct DecodeArgs {
+  const void* q;       // [B][h_k][d_k] dtype
+  const void* k;       // [B][h_k][d_k] dtype
+  const void* v;       // [B][h_v][d_v] dtype
+  const float* g;      // [B][h_v]
+  const float* beta;   // [B][h_v]
+  float* state;        // [B][h_v][d_v][d_k], in place
+  void* o;             // [B][h_v][d_v] dtype
+  int32_t batch, h_k, h_v, d_k, d_v;
+  int dtype;
+  float scale;
+};
+
+struct PrefillArgs {
+  const void* q;            // [T][h_k][d_k] dtype
+  const void* k;            // [T][h_k][d_k] dtype
+  const void* v;            // [T][h_v][d_v] dtype
+  const float* g;           // [T][h_v]
+  const float* beta;        // [T][h_v]
+  const float* state_in;    // [N][h_v][d_v][d_k] or nullptr (zeros)
+  float* state_out;         // [N][h_v][d_v][d_k]
+  void* o;                  // [T][h_v][d_v] dtype
+  const int32_t* cu_seqlens;  // [N+1], device
+  int32_t num_seqs;
+  int64_t total_tokens;
+  int32_t h_k, h_v, d_k, d_v;
+  int dtype;
+  float scale;
+  // Per-sequence split between the two evaluations: a sequence of length L
+  // is handled by the scan when L < min_chunk_len and by the chunked kernel
+  // otherwise.  (0 = chunked takes every sequence; INT32_MAX = scan takes all.)
+  int32_t min_chunk_len;
+  void* workspace;
+  size_t workspace_bytes;
+  int* err;                 // library error word on this device
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_scan(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream);
+size_t chunked_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
+                               int32_t d_k, int32_t d_v);
+bool chunked_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype);
+
+}  // namespace gdn

@@ -1,0 +1,144 @@
+/*
+ * gdn.h — C ABI of the GB300 (sm_103a) Gated DeltaNet recurrence library.
+ *
+ * The operation.  The page "Optimizing on-device inference for Apple Silicon"
+ * (section "Qwen creates three distinct workload shapes") describes the Gated
+ * DeltaNet layer: a fixed-size recurrent matrix state per head, a learned gate
+ * that keeps part of the old state, and a delta update that writes the current
+ * token; each token depends on the state the previous token produced.  The
+ * equation the library evaluates, per value head h and token t, is the gated
+ * delta rule:
+ *
+ *     alpha_t = exp(g_t)
+ *     S_t     = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t     = S_t (scale * q_t)
+ *
+ * The same section says a prefill may either scan tokens directly while
+ * carrying the state or regroup the updates into blocks that expose matrix
+ * work, and that which is faster depends on model dimensions, workload and
+ * hardware: gdn_prefill offers both (GDN_ALGO_SCAN, GDN_ALGO_CHUNKED) and picks
+ * by a measured crossover (GDN_ALGO_AUTO).  Section "Keep the recurrent state
+ * on-chip" fixes the state and its gate to fp32 while q and k may be bf16.
+ * Section "Reduce intermediate and state traffic" fuses the decode-time
+ * recurrent update into one kernel: gdn_decode_step.
+ *
+ * Shapes and layouts (all tensors dense, contiguous, row-major):
+ *   q, k      [T][h_k][d_k]           dtype        (decode: [B][h_k][d_k])
+ *   v, o      [T][h_v][d_v]           dtype        (decode: [B][h_v][d_v])
+ *   g, beta   [T][h_v]                fp32         (decode: [B][h_v])
+ *   state     [N][h_v][d_v][d_k]      fp32         row i = value dim, col j = key dim
+ *   cu_seqlens[N+1]                   int32, device memory
+ * Value head h reads key/query head h / (h_v / h_k): consecutive value heads
+ * share a key head.  d_k and d_v are each one of 16, 32, 64, 128; h_v must be
+ * a multiple of h_k.  g must be finite (alpha = exp(g) may underflow to 0).
+ *
+ * Ownership.  The caller owns every buffer; the library allocates no device
+ * memory in any call below.  Scratch space for gdn_prefill is the caller's
+ * `workspace` (size from gdn_prefill_workspace_size).
+ *
+ * Asynchrony.  Calls are ordered on the caller's `stream` and return after
+ * the launches are enqueued.  Errors that the host can see (NULL pointers,
+ * shapes, dtypes, 16-byte alignment, workspace size) return synchronously and
+ * launch nothing.  Errors only the device can see (inconsistent cu_seqlens)
+ * are recorded in a per-device error word owned by the library; the affected
+ * sequences are skipped, and gdn_stream_status reports and clears the word.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdn_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_NULL_POINTER = 1,      /* a required pointer is NULL */
+  GDN_ERR_INVALID_ARG = 2,       /* negative size, bad enum, partial state overlap */
+  GDN_ERR_UNSUPPORTED_SHAPE = 3, /* d_k/d_v not in {16,32,64,128}, h_v % h_k != 0, T >= 2^31 */
+  GDN_ERR_UNSUPPORTED_DTYPE = 4, /* dtype not supported by the requested algorithm */
+  GDN_ERR_MISALIGNED = 5,        /* a tensor pointer is not 16-byte aligned */
+  GDN_ERR_BAD_CU_SEQLENS = 6,    /* device-detected: cu[0] != 0, decreasing, or cu[N] != T */
+  GDN_ERR_WORKSPACE_TOO_SMALL = 7,
+  GDN_ERR_DEVICE_TIMEOUT = 8,    /* device-detected: a bounded wait expired */
+  GDN_ERR_CUDA = 9               /* a CUDA runtime call failed */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype; /* dtype of q, k, v and o */
+
+typedef enum {
+  GDN_ALGO_AUTO = 0,    /* per sequence: scan below the measured crossover length, else chunked */
+  GDN_ALGO_SCAN = 1,    /* token scan, state rows resident in registers (fp32 and bf16) */
+  GDN_ALGO_CHUNKED = 2  /* chunks of 64 tokens on tcgen05 tensor cores (bf16) */
+} gdn_algo;
+
+/*
+ * gdn_prefill — evaluate the recurrence over N packed sequences.
+ *
+ * Sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.  Its state starts
+ * from state_in[n] (all zeros when state_in is NULL) and its final state is
+ * written to state_out[n]; o[t] = S_t q_t for each of its tokens.  An empty
+ * sequence copies its initial state and writes no output.  state_in may equal
+ * state_out (in-place carry); any other overlap is GDN_ERR_INVALID_ARG.
+ * Output rows of tokens outside every sequence are not written.
+ *
+ * Arguments: q, k, v, o in `dtype`; g, beta, state_in, state_out fp32;
+ * cu_seqlens int32 device pointer of num_seqs+1 entries with cu[0] = 0,
+ * non-decreasing, cu[num_seqs] = total_tokens; scale multiplies q (1 for the
+ * plain reading o_t = S_t q_t).  algo selects the evaluation (see gdn_algo);
+ * GDN_ALGO_CHUNKED with GDN_F32 returns GDN_ERR_UNSUPPORTED_DTYPE.
+ * workspace must hold gdn_prefill_workspace_size(...) bytes (may be NULL when
+ * that size is 0) and is not used after the launches complete.
+ */
+gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, const float* state_in, float* state_out, void* o,
+                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                       float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                       gdn_stream_t stream);
+
+/* Bytes of workspace gdn_prefill needs for these arguments (0 when none). */
+size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
+                                  int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                                  gdn_algo algo);
+
+/*
+ * gdn_decode_step — one token for each of `batch` independent sequences,
+ * state updated in place (one read and one write of every state element).
+ * Same equation and head mapping as gdn_prefill with one token per sequence:
+ * q, k [batch][h_k][d_k], v, o [batch][h_v][d_v] in `dtype`; g, beta
+ * [batch][h_v] fp32; state [batch][h_v][d_v][d_k] fp32.
+ */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, void* o, int32_t batch, int32_t h_k,
+                           int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
+                           gdn_stream_t stream);
+
+/*
+ * gdn_stream_status — synchronise `stream`, then report (and clear) the
+ * current device's error word: GDN_OK, GDN_ERR_BAD_CU_SEQLENS,
+ * GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if the stream reported a CUDA error.
+ */
+gdn_status gdn_stream_status(gdn_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* gdn_status_string(gdn_status status);
+
+/*
+ * gdn_prefill_crossover_tokens — the sequence length at and above which
+ * GDN_ALGO_AUTO uses the chunked evaluation for these head dimensions and
+ * dtype (a table measured on GB300); shorter sequences use the token scan.
+ * Returns INT32_MAX when the chunked evaluation does not support the case.
+ */
+int32_t gdn_prefill_crossover_tokens(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v,
+                                     gdn_dtype dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

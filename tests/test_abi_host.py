@@ -1,0 +1,93 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol that
+include/gdn.h declares, and rejects host-checkable errors without launching
+anything (these calls touch no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_linear_recurrence_gb300 import _lib
+from gated_deltanet_linear_recurrence_gb300.build import build, ROOT
+
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "gdn_prefill" in names and "gdn_decode_step" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in gdn.h but not exported"
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature in the binding"
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.gdn_status_string(code).decode() == name
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=None, state_out=FAKE, o=FAKE,
+             cu=FAKE, n=1, t=64, h_k=1, h_v=1, d_k=16, d_v=16, dtype=1, scale=1.0, algo=1,
+             ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.gdn_prefill(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state_in"],
+                           a["state_out"], a["o"], a["cu"], a["n"], a["t"], a["h_k"], a["h_v"],
+                           a["d_k"], a["d_v"], a["dtype"], a["scale"], a["algo"], a["ws"],
+                           a["ws_bytes"], a["stream"])
+
+
+def test_prefill_host_errors(lib):
+    assert prefill(lib, q=None) == 1                     # NULL
+    assert prefill(lib, cu=None) == 1
+    assert prefill(lib, n=-1) == 2                       # negative
+    assert prefill(lib, algo=7) == 2                     # bad enum
+    assert prefill(lib, dtype=5) == 4
+    assert prefill(lib, d_k=48) == 3                     # head dim not supported
+    assert prefill(lib, h_k=2, h_v=3) == 3               # h_v % h_k
+    assert prefill(lib, t=1 << 31) == 3                  # beyond int32 cu_seqlens
+    assert prefill(lib, k=FAKE + 4) == 5                 # misaligned
+    assert prefill(lib, state_in=FAKE + 16, state_out=FAKE) == 2   # partial overlap
+    assert prefill(lib, n=0) == 0                        # nothing to do: OK, no launch
+    assert prefill(lib, n=0, q=None) == 0
+
+
+def decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE, b=1, h_k=1, h_v=1,
+             d_k=16, d_v=16, dtype=1, scale=1.0, stream=None)
+    a.update(kw)
+    return lib.gdn_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state"], a["o"],
+                               a["b"], a["h_k"], a["h_v"], a["d_k"], a["d_v"], a["dtype"],
+                               a["scale"], a["stream"])
+
+
+def test_decode_host_errors(lib):
+    assert decode(lib, state=None) == 1
+    assert decode(lib, b=-2) == 2
+    assert decode(lib, d_v=8) == 3
+    assert decode(lib, h_k=4, h_v=2) == 3
+    assert decode(lib, dtype=3) == 4
+    assert decode(lib, o=FAKE + 2) == 5
+    assert decode(lib, b=0) == 0
+
+
+def test_workspace_and_crossover_queries(lib):
+    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 1) == 0  # scan needs none
+    x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
+    assert x > 0
+    assert lib.gdn_prefill_crossover_tokens(16, 32, 128, 48, 1) == 2**31 - 1
