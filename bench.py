@@ -200,11 +200,16 @@ def main():
     ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--kernel-only", choices=["prefill", "decode_b256"], default=None,
+                    help="run only this kernel's workload (warmup + steps launches, no JSON); "
+                         "for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_only:
+        return run_kernel_only(args)
 
     import torch
     import torch.distributed as dist
@@ -438,6 +443,39 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
                                   "tok_s": 1 / (ms / 1e3),
                                   "l2": "flushed between steps; 30 calls in one CUDA graph"}
     return out
+
+
+def run_kernel_only(args):
+    """warmup + steps launches of one kernel's workload, for profiler captures."""
+    import torch
+    from gated_deltanet_linear_recurrence_gb300 import (gdn_decode_step, gdn_prefill,
+                                                        gdn_prefill_workspace_size,
+                                                        gdn_stream_status, inputs)
+
+    dev = torch.device("cuda", 0)
+    if args.kernel_only == "decode_b256":
+        w = inputs.WORKLOADS["decode_b256"]
+        d = inputs.make_decode(w["batch"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                               seed=w["seed"])
+        y = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        o = torch.empty_like(y["v"])
+        for _ in range(args.warmup + args.steps):
+            gdn_decode_step(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"], o=o)
+    else:
+        w = inputs.WORKLOADS[WORKLOAD]
+        d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"],
+                                w["dtype"], seed=w["seed"])
+        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        T = sum(w["lengths"])
+        n = gdn_prefill_workspace_size(1, T, w["h_k"], w["h_v"], w["d_k"], w["d_v"],
+                                       torch.bfloat16, args.algo)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                        algo=args.algo, workspace=ws)
+    torch.cuda.synchronize()
+    assert gdn_stream_status() == "GDN_OK"
+    print(f"kernel-only {args.kernel_only}: {args.warmup + args.steps} launches ok", flush=True)
 
 
 if __name__ == "__main__":
