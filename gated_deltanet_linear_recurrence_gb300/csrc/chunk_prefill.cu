@@ -1,14 +1,650 @@
 // chunk_prefill.cu — chunked (WY/UT) prefill on tcgen05 tensor cores.
-// (Not yet available: chunked_supports() reports false, so GDN_ALGO_AUTO uses
-// the token scan and GDN_ALGO_CHUNKED is refused on the host.)
+//
+// Page "Optimizing on-device inference for Apple Silicon", section "Qwen
+// creates three distinct workload shapes": besides scanning tokens while
+// carrying the state, a prefill can regroup the updates into blocks that
+// expose matrix operations and token-level parallelism.  This file is that
+// block form, with blocks (chunks) of C = 64 tokens.  Per chunk of n <= 64
+// tokens, with S the d_v x d_k state at the chunk start, gamma the in-chunk
+// cumulative sum of the log-gates g and Gamma = exp(gamma):
+//
+//   A_ri = beta_r e^{gamma_r - gamma_i} (k_r . k_i)   (i < r)     strictly lower
+//   P_ri =        e^{gamma_r - gamma_i} (q_r . k_i)   (i <= r)
+//   T    = (I + A)^{-1}                               (unit lower triangular)
+//   W    = T diag(beta Gamma) K,   U~ = T diag(beta) V,   U = U~ - W S^T
+//   O    = diag(Gamma) Q S^T + P U
+//   S'   = Gamma_n S + U^T diag(e^{gamma_n - gamma}) K
+//
+// which follows from the row identity u_r = beta_r (v_r - alpha_r S_{r-1} k_r),
+// S_r = alpha_r S_{r-1} + u_r k_r^T unrolled over the chunk; the sequential
+// recurrence and this form agree up to rounding.  The state and the gates stay
+// fp32 ("Keep the recurrent state on-chip"): the state of the CTA's slice
+// lives in TMEM as an fp32 accumulator for the whole sequence and only a bf16
+// copy of it is staged in shared memory as an MMA operand.
+//
+// Work split: one CTA per (sequence, value head, slice of 32 value rows); the
+// CTA walks its sequence's chunks in order.  Inside the CTA three roles run
+// concurrently, handing buffers over through mbarriers:
+//   * producer warp: TMA of the chunk's K, Q (two 64-column boxes each) and
+//     V slice into a ring of 3 stages;
+//   * 8 "prep" warps: everything that does not depend on the state, for the
+//     chunk ahead of the chain: gates, K K^T / Q K^T masks, the triangular
+//     solve, W and U~ (written into double-buffered smem / TMEM);
+//   * 4 "chain" warps: the state-dependent steps of the current chunk:
+//     U = U~ - W S^T, O = Gamma Q S^T + P U, S' = Gamma_n S + K^T (decay U).
+// The key-only work is recomputed by the 4 slices of a head, which keeps
+// slices independent and puts 4x more CTAs on the chain at batch 1.
+//
+// Tensor-core products (bf16 operands, fp32 TMEM accumulators):
+//   prep:  G   = [K;Q] K^T          M=128 N=64 K=128   (rows 0-63: K K^T, 64-127: Q K^T)
+//          W^T = K^T (T b Gamma)^T  M=128 N=64 K=64
+//          U~  = (T b) V_s          M=64  N=32 K=64
+//   chain: O1  = Q S_s^T            M=64  N=32 K=128
+//          U  += (-W) S_s^T         M=64  N=32 K=128
+//          O2  = P U                M=64  N=32 K=64
+//          S^T+= K^T (e^{..} U)     M=128 N=32 K=64    (onto Gamma_n S^T)
+// The triangular solve is fp32 FFMA, in place: 16x16 diagonal blocks by
+// forward substitution, then block rows combined.
+//
+// Partial last chunk: rows n..63 get g = 0 and beta = 0, which makes them an
+// exact no-op (A, W, U~ and U rows vanish, Gamma stays at Gamma_{n-1}); their
+// outputs are not stored.  Inputs must be finite.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
 #include "params.h"
+#include "rows.cuh"
+#include "tc.cuh"
 
 namespace gdn {
+namespace {
 
-bool chunked_supports(int32_t, int32_t, int32_t, int32_t, int) { return false; }
+constexpr int kC = 64;      // chunk length
+constexpr int kDK = 128;    // key dimension handled by this kernel
+constexpr int kDVS = 32;    // value rows per CTA
+constexpr int kChainWarps = 4, kPrepWarps = 8;
+constexpr int kChainThreads = 32 * kChainWarps;   // 128
+constexpr int kPrepThreads = 32 * kPrepWarps;     // 256
+constexpr int kThreads = kChainThreads + kPrepThreads + 32;  // + producer warp = 416
+constexpr int kProducerWarp = kChainWarps + kPrepWarps;      // warp 12
+constexpr uint32_t kBarChain = 1, kBarPrep = 2;               // named barrier ids
+constexpr int kStages = 3;
+
+// Shared-memory layout (byte offsets from a 1024-aligned base).
+constexpr uint32_t kKQBytes = 32768;               // [K;Q] for d_k 0-63, then for 64-127
+constexpr uint32_t kStageBytes = kKQBytes + 4096;  // + V slice [64 tokens][32] bf16
+constexpr uint32_t OFF_STAGE = 0;
+constexpr uint32_t OFF_WN = kStages * kStageBytes;  // 2 x (-W) bf16 [j][r], SW128, 16 KB
+constexpr uint32_t OFF_PP = OFF_WN + 2 * 16384;     // 2 x P bf16 [r][i], SW128, 8 KB
+constexpr uint32_t OFF_TB = OFF_PP + 2 * 8192;      // T diag(b Gamma) [r][i], SW128, 8 KB
+constexpr uint32_t OFF_TA = OFF_TB + 8192;          // T diag(b) [r][i], SW128, 8 KB
+constexpr uint32_t OFF_SS = OFF_TA + 8192;          // S slice bf16 [j][i], SW64, 8 KB
+constexpr uint32_t OFF_UB = OFF_SS + 8192;          // U bf16 [r][i], SW64, 4 KB
+constexpr uint32_t OFF_UK = OFF_UB + 4096;          // decayed U bf16 [r][i], SW64, 4 KB
+constexpr int kLdF = 65;                            // fp32 row stride (conflict-free columns)
+constexpr uint32_t OFF_AF = OFF_UK + 4096;          // A, then T in place: fp32 [64][65]
+constexpr uint32_t OFF_YF = OFF_AF + 64 * kLdF * 4;  // solve scratch fp32 [3][16][17]
+constexpr uint32_t OFF_GATE = OFF_YF + 3 * 16 * 17 * 4;  // 2 x {gamma, Gamma, beta, decay}[64]
+constexpr uint32_t kGateFloats = 4 * 64;
+constexpr uint32_t OFF_MISC = OFF_GATE + 2 * kGateFloats * 4;
+constexpr uint32_t kSmemUsed = OFF_MISC + 256;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(OFF_WN % 1024 == 0 && OFF_PP % 1024 == 0 && OFF_TB % 1024 == 0 &&
+                  OFF_TA % 1024 == 0 && OFF_SS % 512 == 0 && OFF_UB % 512 == 0 &&
+                  OFF_UK % 512 == 0 && kStageBytes % 1024 == 0,
+              "swizzled operands need 1024 (SW128) / 512 (SW64) byte alignment");
+
+// TMEM columns (fp32, 128 lanes each).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_G = 0, TM_WT = 64, TM_U0 = 128, TM_O1 = 192, TM_O2 = 224, TM_S = 256;
+
+// Instruction descriptors.
+constexpr uint32_t ID_G = tc::idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t ID_WT = tc::idesc_bf16_f32(128, 64, true, false);
+constexpr uint32_t ID_UT = tc::idesc_bf16_f32(64, 32, false, true);
+constexpr uint32_t ID_QS = tc::idesc_bf16_f32(64, 32, false, true);
+constexpr uint32_t ID_WS = tc::idesc_bf16_f32(64, 32, true, true);
+constexpr uint32_t ID_PU = tc::idesc_bf16_f32(64, 32, false, true);
+constexpr uint32_t ID_SU = tc::idesc_bf16_f32(128, 32, true, true);
+
+struct ChunkParams {
+  const float* g;
+  const float* beta;
+  const float* state_in;
+  float* state_out;
+  __nv_bfloat16* o;
+  const int32_t* cu;
+  int32_t num_seqs;
+  int64_t total_tokens;
+  int32_t h_k, h_v, d_v;
+  float scale;
+  int32_t min_len;
+  int* err;
+};
+
+// mbarriers in the MISC area
+struct Bars {
+  uint64_t tma_full[kStages];    // producer -> consumers (transaction bytes)
+  uint64_t stage_free[kStages];  // prep + chain -> producer (2 arrivals)
+  uint64_t prep_ready[2];        // prep -> chain: W, P, U~, gates of a chunk ready
+  uint64_t chain_free[2];        // chain -> prep: that buffer set consumed
+  uint64_t mma_prep;             // prep MMA completion
+  uint64_t mma_chain;            // chain MMA completion
+  uint32_t tmem_base;
+};
+static_assert(sizeof(Bars) <= 256, "misc area");
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Store 8 consecutive bf16 values (16 bytes) at a swizzled offset.
+template <int kBits>
+__device__ __forceinline__ void st_chunk(uint8_t* base, uint32_t off, const float* x) {
+  uint4 u;
+  u.x = pack_bf16(x[0], x[1]);
+  u.y = pack_bf16(x[2], x[3]);
+  u.z = pack_bf16(x[4], x[5]);
+  u.w = pack_bf16(x[6], x[7]);
+  *reinterpret_cast<uint4*>(base + tc::swizzle<kBits>(off)) = u;
+}
+
+// Wait on an mbarrier phase; the outcome is made uniform over a named-barrier group.
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint32_t id,
+                                           uint32_t count) {
+  const bool ok = tc::mbar_wait(bar, parity);
+  tc::fence_after_sync();
+  return tc::named_sync_and(id, count, ok);
+}
+
+__device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
+  tc::fence_before_sync();
+  tc::named_sync(id, count);
+  tc::fence_after_sync();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const ChunkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = p.d_v / kDVS;
+  const int s = blockIdx.x % ns;
+  const int h = (blockIdx.x / ns) % p.h_v;
+  const int n = blockIdx.x / (ns * p.h_v);
+  const int hk = h / (p.h_v / p.h_k);
+
+  const int64_t t_beg = p.cu[n], t_end = p.cu[n + 1];
+  const bool bad = t_beg < 0 || t_end < t_beg || t_end > p.total_tokens ||
+                   (n == 0 && t_beg != 0) || (n == p.num_seqs - 1 && t_end != p.total_tokens);
+  if (bad) {
+    if (tid == 0 && h == 0 && s == 0) raise_error(p.err, kErrBadCuSeqlens);
+    return;
+  }
+  const int64_t L = t_end - t_beg;
+  if (L < p.min_len) return;  // the token scan owns this sequence
+
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_MISC);
+  float* AF = reinterpret_cast<float*>(smem + OFF_AF);
+  float* YF = reinterpret_cast<float*>(smem + OFF_YF);
+  const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;  // first state row
+  const int nchunks = (int)((L + kC - 1) / kC);
+
+  if (warp == 0) {
+    tc::tmem_alloc(&bars->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(&bars->tma_full[i], 1);
+      tc::mbar_init(&bars->stage_free[i], 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bars->prep_ready[i], 1);
+      tc::mbar_init(&bars->chain_free[i], 1);
+    }
+    tc::mbar_init(&bars->mma_prep, 1);
+    tc::mbar_init(&bars->mma_chain, 1);
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  bool ok = true;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(&tm_v);
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kStages;
+        if (c >= kStages && !tc::mbar_wait(&bars->stage_free[st], ((c / kStages) - 1) & 1)) {
+          raise_error(p.err, kErrDeviceTimeout);
+          break;
+        }
+        uint8_t* dst = smem + OFF_STAGE + st * kStageBytes;
+        const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
+        uint64_t* fb = &bars->tma_full[st];
+        tc::mbar_arrive_expect_tx(fb, kStageBytes);
+        tc::tma_load_2d(dst, &tm_k, hk * kDK, y, fb);
+        tc::tma_load_2d(dst + 8192, &tm_q, hk * kDK, y, fb);
+        tc::tma_load_2d(dst + 16384, &tm_k, hk * kDK + 64, y, fb);
+        tc::tma_load_2d(dst + 24576, &tm_q, hk * kDK + 64, y, fb);
+        tc::tma_load_2d(dst + kKQBytes, &tm_v, h * p.d_v + s * kDVS, y, fb);
+      }
+    }
+  } else if (warp >= kChainWarps) {
+    // ------------------------------------------------------------ prep
+    const int pt = tid - kChainThreads;  // 0..255
+    const int pw = pt >> 5;              // prep warp 0..7
+    const bool leader = pt == 0;
+    uint32_t mma_phase = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int b = c & 1, st = c % kStages;
+      const uint32_t stg = sbase + OFF_STAGE + st * kStageBytes;
+      float* gate = reinterpret_cast<float*>(smem + OFF_GATE) + b * kGateFloats;
+      float *gam = gate, *Gam = gate + 64, *bet = gate + 128, *dec = gate + 192;
+      const int64_t t0 = t_beg + (int64_t)c * kC;
+      const int nv = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+
+      float gr = 0.f, br = 0.f;
+      if (pt < nv) {
+        gr = p.g[(t0 + pt) * p.h_v + h];
+        br = p.beta[(t0 + pt) * p.h_v + h];
+      }
+      // buffers b were last used by the chain for chunk c-2
+      if (c >= 2) {
+        ok = group_wait(&bars->chain_free[b], ((c >> 1) - 1) & 1, kBarPrep, kPrepThreads);
+        if (!ok) break;
+      }
+      ok = group_wait(&bars->tma_full[st], (c / kStages) & 1, kBarPrep, kPrepThreads);
+      if (!ok) break;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TM_G, tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128), ID_G, kk > 0);
+        }
+        tc::mma_commit(&bars->mma_prep);
+      }
+      // gates: inclusive scan of g over the chunk (prep warps 0 and 1)
+      if (pt < 64) {
+        float x = gr;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(kFullMask, x, off);
+          if (lane >= off) x += y;
+        }
+        if (pt == 31) YF[0] = x;  // scratch is free until the solve
+        gr = x;
+      }
+      tc::named_sync(kBarPrep, kPrepThreads);
+      if (pt < 64) {
+        if (pw == 1) gr += YF[0];
+        gam[pt] = gr;
+        Gam[pt] = tc::fast_exp(gr);
+        bet[pt] = br;
+      }
+      tc::named_sync(kBarPrep, kPrepThreads);
+      if (pt < 64) dec[pt] = tc::fast_exp(gam[kC - 1] - gam[pt]);
+
+      // masks: A (fp32, solve input) from K K^T rows, P (bf16 operand) from Q K^T rows
+      ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
+      ++mma_phase;
+      if (!ok) break;
+      {
+        const int sp = pw & 3, half = pw >> 2;  // TMEM subpartition, column half
+        float a[32];
+        tc::tmem_ld32(tmem + lane_base + TM_G + 32 * half, a);
+        const int m = 32 * sp + lane;
+        const int i0 = 32 * half;
+        if (m < 64) {
+          const int r = m;
+          const float g_r = gam[r], b_r = bet[r];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = i0 + e;
+            AF[r * kLdF + i] = (i < r) ? b_r * tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
+          }
+        } else {
+          const int r = m - 64;
+          const float g_r = gam[r];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = i0 + e;
+            a[e] = (i <= r) ? tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
+          }
+          uint8_t* pp = smem + OFF_PP + b * 8192;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_chunk<3>(pp, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+        }
+      }
+      group_sync(kBarPrep, kPrepThreads);
+
+      // T = (I + A)^{-1}, in place.  Diagonal 16x16 blocks: prep warp w < 4, lane = column.
+      if (pw < 4 && lane < 16) {
+        const int o = 16 * pw, cc = lane;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < r; ++i) acc = fmaf(AF[(o + r) * kLdF + o + i], x[i], acc);
+          x[r] = (r == cc) ? 1.f : ((r > cc) ? -acc : 0.f);
+        }
+        __syncwarp(0x0000ffffu);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) AF[(o + r) * kLdF + o + cc] = x[r];
+      }
+      tc::named_sync(kBarPrep, kPrepThreads);
+      for (int bi = 1; bi < 4; ++bi) {
+        // Y_j = sum_{k=j}^{bi-1} A_{bi,k} T_{k,j}
+        for (int e = pt; e < bi * 256; e += kPrepThreads) {
+          const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+          float acc = 0.f;
+          for (int k = j; k < bi; ++k) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+              acc = fmaf(AF[(16 * bi + rr) * kLdF + 16 * k + m],
+                         AF[(16 * k + m) * kLdF + 16 * j + cc], acc);
+          }
+          YF[(j * 16 + rr) * 17 + cc] = acc;
+        }
+        tc::named_sync(kBarPrep, kPrepThreads);
+        // T_{bi,j} = -T_{bi,bi} Y_j  (overwrites A_{bi,j})
+        for (int e = pt; e < bi * 256; e += kPrepThreads) {
+          const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            acc = fmaf(AF[(16 * bi + rr) * kLdF + 16 * bi + m], YF[(j * 16 + m) * 17 + cc], acc);
+          AF[(16 * bi + rr) * kLdF + 16 * j + cc] = -acc;
+        }
+        tc::named_sync(kBarPrep, kPrepThreads);
+      }
+      {  // operands T diag(b Gamma) (prep threads 0-127) and T diag(b) (128-255)
+        const bool with_gamma = pt < 128;
+        const int r = (pt & 127) >> 1, half = pt & 1;
+        uint8_t* dst = smem + (with_gamma ? OFF_TB : OFF_TA);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = 32 * half + 8 * c8 + e;
+            x[e] = AF[r * kLdF + i] * bet[i] * (with_gamma ? Gam[i] : 1.f);
+          }
+          st_chunk<3>(dst, r * 128 + (4 * half + c8) * 16, x);
+        }
+      }
+      tc::fence_proxy_async();
+      group_sync(kBarPrep, kPrepThreads);
+
+      // W^T = K^T (T b Gamma)^T and U~ = (T b) V on the tensor cores
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tmem + TM_WT, tc::smem_desc(stg + kk * 2048, 16384, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(sbase + OFF_TB + kk * 32, 16, 1024, tc::kLayoutSw128), ID_WT,
+                       kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tmem + TM_U0 + 32 * b,
+                       tc::smem_desc(sbase + OFF_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(stg + kKQBytes + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_UT,
+                       kk > 0);
+        tc::mma_commit(&bars->mma_prep);
+      }
+      ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
+      ++mma_phase;
+      if (!ok) break;
+      {  // -W into the [j][r] operand: thread (subpartition sp, lane) holds W_{r,j}, j = 32 sp + lane
+        const int sp = pw & 3, half = pw >> 2;
+        float w[32];
+        tc::tmem_ld32(tmem + lane_base + TM_WT + 32 * half, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = -w[e];
+        const int j = 32 * sp + lane;
+        uint8_t* wn = smem + OFF_WN + b * 16384;
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(wn, j * 128 + (4 * half + c8) * 16, w + 8 * c8);
+      }
+      tc::fence_proxy_async();
+      group_sync(kBarPrep, kPrepThreads);
+      if (leader) {
+        tc::mbar_arrive(&bars->prep_ready[b]);
+        tc::mbar_arrive(&bars->stage_free[st]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ chain
+    const bool leader = tid == 0;
+    uint32_t mma_phase = 0;
+    const uint32_t ss = sbase + OFF_SS;
+    {  // initial state: thread j holds column j of the slice (rows i = 0..31)
+      float sc[32];
+#pragma unroll
+      for (int i = 0; i < kDVS; ++i)
+        sc[i] = p.state_in ? p.state_in[(srow0 + i) * kDK + tid] : 0.f;
+      if (nchunks == 0) {
+#pragma unroll
+        for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+      } else {
+        tc::tmem_st32(tmem + lane_base + TM_S, sc);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_SS, tid * 64 + c4 * 16, sc + 8 * c4);
+      }
+      tc::fence_proxy_async();
+      group_sync(kBarChain, kChainThreads);
+    }
+    for (int c = 0; c < nchunks; ++c) {
+      const int b = c & 1, st = c % kStages;
+      const uint32_t stg = sbase + OFF_STAGE + st * kStageBytes;
+      const float* gate = reinterpret_cast<const float*>(smem + OFF_GATE) + b * kGateFloats;
+      const int64_t t0 = t_beg + (int64_t)c * kC;
+      const int nv = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
+
+      ok = group_wait(&bars->prep_ready[b], (c >> 1) & 1, kBarChain, kChainThreads);
+      if (!ok) break;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(tmem + TM_U0 + 32 * b,
+                       tc::smem_desc(sbase + OFF_WN + b * 16384 + kk * 2048, 16384, 1024,
+                                     tc::kLayoutSw128),
+                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_WS, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + 8192 + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TM_O1, tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_QS, kk > 0);
+        }
+        tc::mma_commit(&bars->mma_chain);
+      }
+      // gates this thread needs, read before the buffer set is released
+      const int r = 16 * warp + lane;  // M=64 accumulator row held by lanes 0-15
+      const float Gam_n = gate[64 + kC - 1];
+      const float Gam_r = gate[64 + (r & 63)];
+      const float dec_r = gate[192 + (r & 63)];
+      {  // S <- Gamma_n S (the update MMA accumulates onto it)
+        float sc[32];
+        tc::tmem_ld32(tmem + lane_base + TM_S, sc);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
+        tc::tmem_st32(tmem + lane_base + TM_S, sc);
+      }
+      ok = group_wait(&bars->mma_chain, mma_phase & 1, kBarChain, kChainThreads);
+      ++mma_phase;
+      if (!ok) break;
+      {
+        float u[32];
+        tc::tmem_ld32(tmem + lane_base + TM_U0 + 32 * b, u);
+        if (lane < 16) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UB, r * 64 + c4 * 16, u + 8 * c4);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] *= dec_r;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UK, r * 64 + c4 * 16, u + 8 * c4);
+        }
+      }
+      tc::fence_proxy_async();
+      group_sync(kBarChain, kChainThreads);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tmem + TM_O2,
+                       tc::smem_desc(sbase + OFF_PP + b * 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(sbase + OFF_UB + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_PU,
+                       kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tmem + TM_S, tc::smem_desc(stg + kk * 2048, 16384, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(sbase + OFF_UK + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_SU,
+                       1);
+        tc::mma_commit(&bars->mma_chain);
+      }
+      ok = group_wait(&bars->mma_chain, mma_phase & 1, kBarChain, kChainThreads);
+      ++mma_phase;
+      if (!ok) break;
+      if (leader) {  // W, P, U~ and gates of buffer b, and the stage, are consumed
+        tc::mbar_arrive(&bars->chain_free[b]);
+        tc::mbar_arrive(&bars->stage_free[st]);
+      }
+      {
+        float o1[32], o2[32];
+        tc::tmem_ld32(tmem + lane_base + TM_O1, o1);
+        tc::tmem_ld32(tmem + lane_base + TM_O2, o2);
+        if (lane < 16 && r < nv) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0 + r) * p.h_v + h) * (int64_t)p.d_v +
+                                                s * kDVS);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint4 q4;
+            q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
+            q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
+            q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
+            q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
+            dst[c4] = q4;
+          }
+        }
+        float sc[32];
+        tc::tmem_ld32(tmem + lane_base + TM_S, sc);
+        if (c == nchunks - 1) {
+#pragma unroll
+          for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            st_chunk<2>(smem + OFF_SS, tid * 64 + c4 * 16, sc + 8 * c4);
+        }
+      }
+      tc::fence_proxy_async();
+      group_sync(kBarChain, kChainThreads);
+    }
+  }
+  if (!ok && (tid == 0 || tid == kChainThreads)) raise_error(p.err, kErrDeviceTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunked_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
+  return dtype == kBF16 && d_k == kDK && d_v >= kDVS && d_v % kDVS == 0 && h_k > 0 &&
+         h_v % h_k == 0;
+}
 
 size_t chunked_workspace_bytes(int32_t, int64_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
-cudaError_t launch_chunked(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  if (!chunked_supports(a.h_k, a.h_v, a.d_k, a.d_v, a.dtype)) return cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv;
+  const uint64_t rows = a.total_tokens > 0 ? (uint64_t)a.total_tokens : 1;
+  // With no tokens every sequence is empty and no TMA is issued; the maps still
+  // need a valid (non-null) address, so point them at the state buffer.
+  const void* qp = a.total_tokens > 0 ? a.q : a.state_out;
+  const void* kp = a.total_tokens > 0 ? a.k : a.state_out;
+  const void* vp = a.total_tokens > 0 ? a.v : a.state_out;
+  if (!encode_2d(&mq, qp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, kDVS, kC, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(chunk_prefill_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  ChunkParams p;
+  p.g = a.g;
+  p.beta = a.beta;
+  p.state_in = a.state_in;
+  p.state_out = a.state_out;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.cu = a.cu_seqlens;
+  p.num_seqs = a.num_seqs;
+  p.total_tokens = a.total_tokens;
+  p.h_k = a.h_k;
+  p.h_v = a.h_v;
+  p.d_v = a.d_v;
+  p.scale = a.scale;
+  p.min_len = a.min_chunk_len;
+  p.err = a.err;
+  const int64_t grid = (int64_t)a.num_seqs * a.h_v * (a.d_v / kDVS);
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  chunk_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
 
 }  // namespace gdn
