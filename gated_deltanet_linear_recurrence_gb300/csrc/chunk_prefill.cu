@@ -25,26 +25,32 @@
 // Work split: one CTA per (sequence, value head, slice of 32 value rows); the
 // CTA walks its sequence's chunks in order.  Inside the CTA three roles run
 // concurrently, handing buffers over through mbarriers:
-//   * producer warp: TMA of the chunk's K, Q (two 64-column boxes each) and
+//   * producer warp: TMA of the chunk's Q, K (two 64-column boxes each) and
 //     V slice into a ring of 3 stages;
-//   * 8 "prep" warps: everything that does not depend on the state, for the
-//     chunk ahead of the chain: gates, K K^T / Q K^T masks, the triangular
-//     solve, W and U~ (written into double-buffered smem / TMEM);
-//   * 4 "chain" warps: the state-dependent steps of the current chunk:
-//     U = U~ - W S^T, O = Gamma Q S^T + P U, S' = Gamma_n S + K^T (decay U).
-// The key-only work is recomputed by the 4 slices of a head, which keeps
-// slices independent and puts 4x more CTAs on the chain at batch 1.
+//   * 8 "prep" warps: everything that does not depend on the state, one chunk
+//     ahead of the chain: gates, Q K^T / K K^T masks, the triangular solve,
+//     W (written next to Q in the stage) and U~ (into double-buffered TMEM);
+//   * 4 "chain" warps: the state-dependent steps of the current chunk.
+// Measured on GB300, a dependent K=16 step of tcgen05.mma costs about 60-70
+// cycles whatever N (up to 128) and the tensor pipe runs MMAs one at a time,
+// so the kernel is organised to issue few, wide MMAs: [-W; Q] share one M=128
+// operand, and the state update (on the critical path) is issued before the
+// P U product.  The key-only work is recomputed by the 4 slices of a head,
+// which keeps slices independent and puts 4x more CTAs on the chain at batch 1.
 //
-// Tensor-core products (bf16 operands, fp32 TMEM accumulators):
-//   prep:  G   = [K;Q] K^T          M=128 N=64 K=128   (rows 0-63: K K^T, 64-127: Q K^T)
-//          W^T = K^T (T b Gamma)^T  M=128 N=64 K=64
-//          U~  = (T b) V_s          M=64  N=32 K=64
-//   chain: O1  = Q S_s^T            M=64  N=32 K=128
-//          U  += (-W) S_s^T         M=64  N=32 K=128
-//          O2  = P U                M=64  N=32 K=64
-//          S^T+= K^T (e^{..} U)     M=128 N=32 K=64    (onto Gamma_n S^T)
-// The triangular solve is fp32 FFMA, in place: 16x16 diagonal blocks by
-// forward substitution, then block rows combined.
+// Tensor-core products (bf16 operands, fp32 TMEM accumulators; an operand
+// written [X; Y] is an M=128 operand whose X rows are don't-care):
+//   prep:  G  = [Q;K] K^T          M=128 N=64  K=128  (rows 0-63: Q K^T, 64-127: K K^T)
+//          W  = [T b Gamma; .] K   M=128 N=128 K=64
+//          U~ = [T b; .] V_s       M=128 N=32  K=64
+//   chain: D  = [-W; Q] S_s^T      M=128 N=32  K=128  (rows 0-63: -W S^T, 64-127: Q S^T)
+//          S^T += K^T (e^{..} U)   M=128 N=32  K=64   (onto Gamma_n S^T)
+//          O2 = [.; P] U           M=128 N=32  K=64
+// then U = U~ + D_top and O = Gamma D_bottom + O2.  The triangular solve runs
+// in place: 16x16 diagonal blocks by fp32 forward substitution, then 32x32 and
+// 64x64 block combinations whose 16-32 wide products use warp-level tf32
+// tensor-core instructions (too small for the 64-row tcgen05 shapes, and on
+// the prep warps' critical path).
 //
 // Partial last chunk: rows n..63 get g = 0 and beta = 0, which makes them an
 // exact no-op (A, W, U~ and U rows vanish, Gamma stays at Gamma_{n-1}); their
@@ -75,42 +81,50 @@ constexpr uint32_t kBarChain = 1, kBarPrep = 2;               // named barrier i
 constexpr int kStages = 3;
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
-constexpr uint32_t kKQBytes = 32768;               // [K;Q] for d_k 0-63, then for 64-127
-constexpr uint32_t kStageBytes = kKQBytes + 4096;  // + V slice [64 tokens][32] bf16
+// A stage holds, per 64-wide half kb of d_k, [ -W | Q | K ] (8 KB each, K-major
+// SW128 rows of 128 B): Q and K come from TMA, -W is written by the prep warps,
+// so [-W; Q] and [Q; K] are both contiguous 128-row MMA operands.  Then the
+// V slice [64 tokens][32] (SW64).
+constexpr uint32_t kHalfBytes = 3 * 8192;
+constexpr uint32_t kStageBytes = 2 * kHalfBytes + 4096;
+constexpr uint32_t ST_W = 0, ST_Q = 8192, ST_K = 16384, ST_V = 2 * kHalfBytes;
+constexpr uint32_t kTmaBytes = 4 * 8192 + 4096;
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_WN = kStages * kStageBytes;  // 2 x (-W) bf16 [j][r], SW128, 16 KB
-constexpr uint32_t OFF_PP = OFF_WN + 2 * 16384;     // 2 x P bf16 [r][i], SW128, 8 KB
-constexpr uint32_t OFF_TB = OFF_PP + 2 * 8192;      // T diag(b Gamma) [r][i], SW128, 8 KB
-constexpr uint32_t OFF_TA = OFF_TB + 8192;          // T diag(b) [r][i], SW128, 8 KB
-constexpr uint32_t OFF_SS = OFF_TA + 8192;          // S slice bf16 [j][i], SW64, 8 KB
+// TB, TA, P0, P1 are contiguous: the 64 rows after TB / TA / P0 are valid
+// smem, so each can be the upper half of an M=128 operand whose lower half is
+// never read back.
+constexpr uint32_t OFF_TB = kStages * kStageBytes;  // T diag(b Gamma) bf16 [r][i], SW128
+constexpr uint32_t OFF_TA = OFF_TB + 8192;          // T diag(b) bf16 [r][i], SW128
+constexpr uint32_t OFF_PP = OFF_TA + 8192;          // 2 x P bf16 [r][i], SW128
+constexpr uint32_t OFF_SS = OFF_PP + 2 * 8192;      // S slice bf16 [j][i], SW64, 8 KB
 constexpr uint32_t OFF_UB = OFF_SS + 8192;          // U bf16 [r][i], SW64, 4 KB
 constexpr uint32_t OFF_UK = OFF_UB + 4096;          // decayed U bf16 [r][i], SW64, 4 KB
-constexpr int kLdF = 65;                            // fp32 row stride (conflict-free columns)
-constexpr uint32_t OFF_AF = OFF_UK + 4096;          // A, then T in place: fp32 [64][65]
-constexpr uint32_t OFF_YF = OFF_AF + 64 * kLdF * 4;  // solve scratch fp32 [3][16][17]
-constexpr uint32_t OFF_GATE = OFF_YF + 3 * 16 * 17 * 4;  // 2 x {gamma, Gamma, beta, decay}[64]
+constexpr int kLdM = 68;                            // A, then T in place: fp32 [r][i]
+constexpr uint32_t OFF_MF = OFF_UK + 4096;
+constexpr int kLdY = 40;                            // solve scratch fp32 [32][40], aliases TB
+constexpr uint32_t OFF_YF = OFF_TB;
+constexpr uint32_t OFF_GATE = OFF_MF + 64 * kLdM * 4;  // 2 x {gamma, Gamma, beta, decay}[64]
 constexpr uint32_t kGateFloats = 4 * 64;
 constexpr uint32_t OFF_MISC = OFF_GATE + 2 * kGateFloats * 4;
 constexpr uint32_t kSmemUsed = OFF_MISC + 256;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(OFF_WN % 1024 == 0 && OFF_PP % 1024 == 0 && OFF_TB % 1024 == 0 &&
-                  OFF_TA % 1024 == 0 && OFF_SS % 512 == 0 && OFF_UB % 512 == 0 &&
-                  OFF_UK % 512 == 0 && kStageBytes % 1024 == 0,
+static_assert(OFF_TB % 1024 == 0 && OFF_PP % 1024 == 0 && OFF_SS % 512 == 0 &&
+                  OFF_UB % 512 == 0 && OFF_UK % 512 == 0 && kStageBytes % 1024 == 0 &&
+                  32 * kLdY * 4 <= 8192 && (kLdM * 4) % 16 == 0,
               "swizzled operands need 1024 (SW128) / 512 (SW64) byte alignment");
 
 // TMEM columns (fp32, 128 lanes each).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_G = 0, TM_WT = 64, TM_U0 = 128, TM_O1 = 192, TM_O2 = 224, TM_S = 256;
+constexpr uint32_t TM_G = 0, TM_W = 64, TM_U0 = 192, TM_D0 = 256, TM_O2 = 320, TM_S = 352;
 
 // Instruction descriptors.
-constexpr uint32_t ID_G = tc::idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t ID_WT = tc::idesc_bf16_f32(128, 64, true, false);
-constexpr uint32_t ID_UT = tc::idesc_bf16_f32(64, 32, false, true);
-constexpr uint32_t ID_QS = tc::idesc_bf16_f32(64, 32, false, true);
-constexpr uint32_t ID_WS = tc::idesc_bf16_f32(64, 32, true, true);
-constexpr uint32_t ID_PU = tc::idesc_bf16_f32(64, 32, false, true);
-constexpr uint32_t ID_SU = tc::idesc_bf16_f32(128, 32, true, true);
+constexpr uint32_t ID_G = tc::idesc_bf16_f32(128, 64, false, false);   // [Q;K] K^T
+constexpr uint32_t ID_W = tc::idesc_bf16_f32(128, 128, false, true);   // [TB;.] K
+constexpr uint32_t ID_UT = tc::idesc_bf16_f32(128, 32, false, true);   // [TA;.] V_s
+constexpr uint32_t ID_WQ = tc::idesc_bf16_f32(128, 32, false, true);   // [-W;Q] S_s^T
+constexpr uint32_t ID_SU = tc::idesc_bf16_f32(128, 32, true, true);    // K^T (decay U)
+constexpr uint32_t ID_PU = tc::idesc_bf16_f32(128, 32, false, true);   // [.;P] U
 
 struct ChunkParams {
   const float* g;
@@ -131,10 +145,11 @@ struct ChunkParams {
 struct Bars {
   uint64_t tma_full[kStages];    // producer -> consumers (transaction bytes)
   uint64_t stage_free[kStages];  // prep + chain -> producer (2 arrivals)
-  uint64_t prep_ready[2];        // prep -> chain: W, P, U~, gates of a chunk ready
+  uint64_t prep_ready[2];        // prep -> chain: -W, P, U~, gates of a chunk ready
   uint64_t chain_free[2];        // chain -> prep: that buffer set consumed
   uint64_t mma_prep;             // prep MMA completion
-  uint64_t mma_chain;            // chain MMA completion
+  uint64_t mma_chain;            // chain MMA completion ([-W;Q] S^T, then the S update)
+  uint64_t mma_out;              // chain MMA completion (P U)
   uint32_t tmem_base;
 };
 static_assert(sizeof(Bars) <= 256, "misc area");
@@ -169,6 +184,103 @@ __device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
   tc::fence_after_sync();
 }
 
+// Warp-level tf32 tensor-core product for the small block products of the
+// triangular solve: C (16 x 8) = A (16 x K) B (K x 8), fp32 accumulation.
+// Fragment layout of mma.m16n8k8 (PTX ISA): g = lane / 4, t = lane % 4;
+// A: (g, t), (g+8, t), (g, t+4), (g+8, t+4); B: (t, g), (t+4, g);
+// C: (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+template <int K>
+__device__ __forceinline__ void warp_mma_16x8(float (&c)[4], const float* A, int lda,
+                                              const float* B, int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  c[0] = c[1] = c[2] = c[3] = 0.f;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    const uint32_t a0 = to_tf32(A[g * lda + k0 + t]);
+    const uint32_t a1 = to_tf32(A[(g + 8) * lda + k0 + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + k0 + t + 4]);
+    const uint32_t a3 = to_tf32(A[(g + 8) * lda + k0 + t + 4]);
+    const uint32_t b0 = to_tf32(B[(k0 + t) * ldb + g]);
+    const uint32_t b1 = to_tf32(B[(k0 + t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+// Store a C fragment (scaled by s) into a row-major fp32 block.
+__device__ __forceinline__ void store_16x8(float* C, int ldc, const float (&c)[4], float s,
+                                           int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  C[g * ldc + 2 * t] = s * c[0];
+  C[g * ldc + 2 * t + 1] = s * c[1];
+  C[(g + 8) * ldc + 2 * t] = s * c[2];
+  C[(g + 8) * ldc + 2 * t + 1] = s * c[3];
+}
+
+// T = (I + A)^{-1}, in place, for the strictly lower 64x64 A held row-major in
+// MF (row stride kLdM; its strictly upper part is zero).  Three levels:
+// 16x16 diagonal blocks by forward substitution (fp32 FFMA), then 32x32 blocks
+// as [[T0, 0], [-T1 A10 T0, T1]], then the 64x64 matrix the same way; the block
+// products of the last two levels run on the warp tensor cores in tf32.  Each
+// level only overwrites blocks that later levels read as T.
+__device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt, int lane) {
+  const int pw = pt >> 5;
+  if (pw < 2) {  // level 1: warp pw handles diagonal blocks 2pw, 2pw+1; lane = column
+    const int blk = 2 * pw + (lane >> 4), cc = lane & 15, o = 16 * blk;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) {
+        const float av = MF[(o + r) * kLdM + o + i];
+        if (i & 1) a1 = fmaf(av, x[i], a1); else a0 = fmaf(av, x[i], a0);
+      }
+      x[r] = (r == cc) ? 1.f : ((r > cc) ? -(a0 + a1) : 0.f);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 16; ++r) MF[(o + r) * kLdM + o + cc] = x[r];
+  }
+  tc::named_sync(kBarPrep, kPrepThreads);
+  // level 2: pairs (0,1) and (2,3): Y = A10 T0 (warps 0-3: pair, 8-column tile)
+  if (pw < 4) {
+    const int pr = pw >> 1, nt = pw & 1, o0 = 32 * pr, o1 = o0 + 16;
+    float c[4];
+    warp_mma_16x8<16>(c, MF + o1 * kLdM + o0, kLdM, MF + o0 * kLdM + o0 + 8 * nt, kLdM, lane);
+    store_16x8(YF + (16 * pr) * kLdY + 8 * nt, kLdY, c, 1.f, lane);
+  }
+  tc::named_sync(kBarPrep, kPrepThreads);
+  if (pw < 4) {  // T10 = -T1 Y
+    const int pr = pw >> 1, nt = pw & 1, o0 = 32 * pr, o1 = o0 + 16;
+    float c[4];
+    warp_mma_16x8<16>(c, MF + o1 * kLdM + o1, kLdM, YF + (16 * pr) * kLdY + 8 * nt, kLdY, lane);
+    store_16x8(MF + o1 * kLdM + o0 + 8 * nt, kLdM, c, -1.f, lane);
+  }
+  tc::named_sync(kBarPrep, kPrepThreads);
+  {  // level 3: Y = A_BL T_TL (32x32x32); warp pw: rows 16 (pw>>2), columns 8 (pw&3)
+    const int mt = pw >> 2, nt = pw & 3;
+    float c[4];
+    warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM, kLdM, MF + 8 * nt, kLdM, lane);
+    store_16x8(YF + (16 * mt) * kLdY + 8 * nt, kLdY, c, 1.f, lane);
+  }
+  tc::named_sync(kBarPrep, kPrepThreads);
+  {  // T_BL = -T_BR Y
+    const int mt = pw >> 2, nt = pw & 3;
+    float c[4];
+    warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM + 32, kLdM, YF + 8 * nt, kLdY, lane);
+    store_16x8(MF + (32 + 16 * mt) * kLdM + 8 * nt, kLdM, c, -1.f, lane);
+  }
+  tc::named_sync(kBarPrep, kPrepThreads);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -194,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (L < p.min_len) return;  // the token scan owns this sequence
 
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_MISC);
-  float* AF = reinterpret_cast<float*>(smem + OFF_AF);
+  float* MF = reinterpret_cast<float*>(smem + OFF_MF);
   float* YF = reinterpret_cast<float*>(smem + OFF_YF);
   const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;  // first state row
   const int nchunks = (int)((L + kC - 1) / kC);
@@ -214,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&bars->mma_prep, 1);
     tc::mbar_init(&bars->mma_chain, 1);
+    tc::mbar_init(&bars->mma_out, 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -239,23 +352,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = smem + OFF_STAGE + st * kStageBytes;
         const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
         uint64_t* fb = &bars->tma_full[st];
-        tc::mbar_arrive_expect_tx(fb, kStageBytes);
-        tc::tma_load_2d(dst, &tm_k, hk * kDK, y, fb);
-        tc::tma_load_2d(dst + 8192, &tm_q, hk * kDK, y, fb);
-        tc::tma_load_2d(dst + 16384, &tm_k, hk * kDK + 64, y, fb);
-        tc::tma_load_2d(dst + 24576, &tm_q, hk * kDK + 64, y, fb);
-        tc::tma_load_2d(dst + kKQBytes, &tm_v, h * p.d_v + s * kDVS, y, fb);
+        tc::mbar_arrive_expect_tx(fb, kTmaBytes);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          tc::tma_load_2d(dst + kb * kHalfBytes + ST_Q, &tm_q, hk * kDK + 64 * kb, y, fb);
+          tc::tma_load_2d(dst + kb * kHalfBytes + ST_K, &tm_k, hk * kDK + 64 * kb, y, fb);
+        }
+        tc::tma_load_2d(dst + ST_V, &tm_v, h * p.d_v + s * kDVS, y, fb);
       }
     }
   } else if (warp >= kChainWarps) {
     // ------------------------------------------------------------ prep
     const int pt = tid - kChainThreads;  // 0..255
     const int pw = pt >> 5;              // prep warp 0..7
+    const int sp = pw & 3;               // TMEM subpartition of this warp
     const bool leader = pt == 0;
     uint32_t mma_phase = 0;
     for (int c = 0; c < nchunks; ++c) {
       const int b = c & 1, st = c % kStages;
       const uint32_t stg = sbase + OFF_STAGE + st * kStageBytes;
+      uint8_t* stg_ptr = smem + OFF_STAGE + st * kStageBytes;
       float* gate = reinterpret_cast<float*>(smem + OFF_GATE) + b * kGateFloats;
       float *gam = gate, *Gam = gate + 64, *bet = gate + 128, *dec = gate + 192;
       const int64_t t0 = t_beg + (int64_t)c * kC;
@@ -273,12 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = group_wait(&bars->tma_full[st], (c / kStages) & 1, kBarPrep, kPrepThreads);
       if (!ok) break;
-      if (leader) {
+      if (leader) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          tc::mma_bf16(tmem + TM_G, tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128), ID_G, kk > 0);
+          const uint32_t ko = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TM_G, tc::smem_desc(stg + ko + ST_Q, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(stg + ko + ST_K, 16, 1024, tc::kLayoutSw128), ID_G, kk > 0);
         }
         tc::mma_commit(&bars->mma_prep);
       }
@@ -290,12 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float y = __shfl_up_sync(kFullMask, x, off);
           if (lane >= off) x += y;
         }
-        if (pt == 31) YF[0] = x;  // scratch is free until the solve
+        if (pt == 31) MF[0] = x;  // scratch is free until the masks
         gr = x;
       }
       tc::named_sync(kBarPrep, kPrepThreads);
       if (pt < 64) {
-        if (pw == 1) gr += YF[0];
+        if (pw == 1) gr += MF[0];
         gam[pt] = gr;
         Gam[pt] = tc::fast_exp(gr);
         bet[pt] = br;
@@ -303,26 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::named_sync(kBarPrep, kPrepThreads);
       if (pt < 64) dec[pt] = tc::fast_exp(gam[kC - 1] - gam[pt]);
 
-      // masks: A (fp32, solve input) from K K^T rows, P (bf16 operand) from Q K^T rows
+      // masks: P (bf16 operand) from rows 0-63, A (fp32, solve input) from rows 64-127
       ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
       ++mma_phase;
       if (!ok) break;
       {
-        const int sp = pw & 3, half = pw >> 2;  // TMEM subpartition, column half
+        const int half = pw >> 2;  // column half
         float a[32];
         tc::tmem_ld32(tmem + lane_base + TM_G + 32 * half, a);
-        const int m = 32 * sp + lane;
         const int i0 = 32 * half;
-        if (m < 64) {
-          const int r = m;
-          const float g_r = gam[r], b_r = bet[r];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = i0 + e;
-            AF[r * kLdF + i] = (i < r) ? b_r * tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
-          }
-        } else {
-          const int r = m - 64;
+        if (sp < 2) {
+          const int r = 32 * sp + lane;
           const float g_r = gam[r];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -333,97 +440,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8)
             st_chunk<3>(pp, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+        } else {
+          const int r = 32 * (sp - 2) + lane;
+          const float g_r = gam[r], b_r = bet[r];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = i0 + e;
+            MF[r * kLdM + i] = (i < r) ? b_r * tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
+          }
         }
       }
       group_sync(kBarPrep, kPrepThreads);
 
-      // T = (I + A)^{-1}, in place.  Diagonal 16x16 blocks: prep warp w < 4, lane = column.
-      if (pw < 4 && lane < 16) {
-        const int o = 16 * pw, cc = lane;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < r; ++i) acc = fmaf(AF[(o + r) * kLdF + o + i], x[i], acc);
-          x[r] = (r == cc) ? 1.f : ((r > cc) ? -acc : 0.f);
-        }
-        __syncwarp(0x0000ffffu);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) AF[(o + r) * kLdF + o + cc] = x[r];
-      }
-      tc::named_sync(kBarPrep, kPrepThreads);
-      for (int bi = 1; bi < 4; ++bi) {
-        // Y_j = sum_{k=j}^{bi-1} A_{bi,k} T_{k,j}
-        for (int e = pt; e < bi * 256; e += kPrepThreads) {
-          const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          float acc = 0.f;
-          for (int k = j; k < bi; ++k) {
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-              acc = fmaf(AF[(16 * bi + rr) * kLdF + 16 * k + m],
-                         AF[(16 * k + m) * kLdF + 16 * j + cc], acc);
-          }
-          YF[(j * 16 + rr) * 17 + cc] = acc;
-        }
-        tc::named_sync(kBarPrep, kPrepThreads);
-        // T_{bi,j} = -T_{bi,bi} Y_j  (overwrites A_{bi,j})
-        for (int e = pt; e < bi * 256; e += kPrepThreads) {
-          const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          float acc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            acc = fmaf(AF[(16 * bi + rr) * kLdF + 16 * bi + m], YF[(j * 16 + m) * 17 + cc], acc);
-          AF[(16 * bi + rr) * kLdF + 16 * j + cc] = -acc;
-        }
-        tc::named_sync(kBarPrep, kPrepThreads);
-      }
+      unit_lower_inverse(MF, YF, pt, lane);
+
       {  // operands T diag(b Gamma) (prep threads 0-127) and T diag(b) (128-255)
         const bool with_gamma = pt < 128;
         const int r = (pt & 127) >> 1, half = pt & 1;
         uint8_t* dst = smem + (with_gamma ? OFF_TB : OFF_TA);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
-          float x[8];
+          const int i0 = 32 * half + 8 * c8;
+          const float4 m0 = *reinterpret_cast<const float4*>(MF + r * kLdM + i0);
+          const float4 m1 = *reinterpret_cast<const float4*>(MF + r * kLdM + i0 + 4);
+          float x[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int i = 32 * half + 8 * c8 + e;
-            x[e] = AF[r * kLdF + i] * bet[i] * (with_gamma ? Gam[i] : 1.f);
-          }
+          for (int e = 0; e < 8; ++e) x[e] *= bet[i0 + e] * (with_gamma ? Gam[i0 + e] : 1.f);
           st_chunk<3>(dst, r * 128 + (4 * half + c8) * 16, x);
         }
       }
       tc::fence_proxy_async();
       group_sync(kBarPrep, kPrepThreads);
 
-      // W^T = K^T (T b Gamma)^T and U~ = (T b) V on the tensor cores
+      // W = T b Gamma K and U~ = T b V on the tensor cores (rows 0-63 of M=128)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tmem + TM_WT, tc::smem_desc(stg + kk * 2048, 16384, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(sbase + OFF_TB + kk * 32, 16, 1024, tc::kLayoutSw128), ID_WT,
-                       kk > 0);
+          tc::mma_bf16(tmem + TM_W, tc::smem_desc(sbase + OFF_TB + kk * 32, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(stg + ST_K + kk * 2048, kHalfBytes, 1024, tc::kLayoutSw128),
+                       ID_W, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_bf16(tmem + TM_U0 + 32 * b,
                        tc::smem_desc(sbase + OFF_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(stg + kKQBytes + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_UT,
+                       tc::smem_desc(stg + ST_V + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_UT,
                        kk > 0);
         tc::mma_commit(&bars->mma_prep);
       }
       ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
       ++mma_phase;
       if (!ok) break;
-      {  // -W into the [j][r] operand: thread (subpartition sp, lane) holds W_{r,j}, j = 32 sp + lane
-        const int sp = pw & 3, half = pw >> 2;
+      if (sp < 2) {  // -W rows r = lanes 0-63 into the stage's W slots (K-major)
+        const int half = pw >> 2, r = 32 * sp + lane;
         float w[32];
-        tc::tmem_ld32(tmem + lane_base + TM_WT + 32 * half, w);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = -w[e];
-        const int j = 32 * sp + lane;
-        uint8_t* wn = smem + OFF_WN + b * 16384;
+        for (int q2 = 0; q2 < 2; ++q2) {
+          tc::tmem_ld32(tmem + lane_base + TM_W + 64 * half + 32 * q2, w);
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(wn, j * 128 + (4 * half + c8) * 16, w + 8 * c8);
+          for (int e = 0; e < 32; ++e) w[e] = -w[e];
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_chunk<3>(stg_ptr + half * kHalfBytes + ST_W, r * 128 + (4 * q2 + c8) * 16,
+                        w + 8 * c8);
+        }
       }
       tc::fence_proxy_async();
       group_sync(kBarPrep, kPrepThreads);
@@ -435,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ chain
     const bool leader = tid == 0;
-    uint32_t mma_phase = 0;
+    uint32_t chain_phase = 0, out_phase = 0;
     const uint32_t ss = sbase + OFF_SS;
     {  // initial state: thread j holds column j of the slice (rows i = 0..31)
       float sc[32];
@@ -462,26 +541,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       ok = group_wait(&bars->prep_ready[b], (c >> 1) & 1, kBarChain, kChainThreads);
       if (!ok) break;
-      if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16(tmem + TM_U0 + 32 * b,
-                       tc::smem_desc(sbase + OFF_WN + b * 16384 + kk * 2048, 16384, 1024,
-                                     tc::kLayoutSw128),
-                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_WS, 1);
+      if (leader) {  // D = [-W; Q] S_s^T: rows 0-63 -W S^T, rows 64-127 Q S^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * 16384 + 8192 + (kk & 3) * 32;
-          tc::mma_bf16(tmem + TM_O1, tc::smem_desc(stg + ko, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_QS, kk > 0);
+          const uint32_t ko = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TM_D0 + 32 * b,
+                       tc::smem_desc(stg + ko + ST_W, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_WQ, kk > 0);
         }
         tc::mma_commit(&bars->mma_chain);
       }
       // gates this thread needs, read before the buffer set is released
-      const int r = 16 * warp + lane;  // M=64 accumulator row held by lanes 0-15
+      const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
       const float Gam_n = gate[64 + kC - 1];
-      const float Gam_r = gate[64 + (r & 63)];
-      const float dec_r = gate[192 + (r & 63)];
+      const float dec_r = gate[192 + rl];
+      const float Gam_r = gate[64 + rl];
       {  // S <- Gamma_n S (the update MMA accumulates onto it)
         float sc[32];
         tc::tmem_ld32(tmem + lane_base + TM_S, sc);
@@ -489,63 +563,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
         tc::tmem_st32(tmem + lane_base + TM_S, sc);
       }
-      ok = group_wait(&bars->mma_chain, mma_phase & 1, kBarChain, kChainThreads);
-      ++mma_phase;
+      ok = group_wait(&bars->mma_chain, chain_phase & 1, kBarChain, kChainThreads);
+      ++chain_phase;
       if (!ok) break;
-      {
-        float u[32];
+      if (warp < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
+        float u[32], d[32];
         tc::tmem_ld32(tmem + lane_base + TM_U0 + 32 * b, u);
-        if (lane < 16) {
+        tc::tmem_ld32(tmem + lane_base + TM_D0 + 32 * b, d);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UB, r * 64 + c4 * 16, u + 8 * c4);
+        for (int i = 0; i < 32; ++i) u[i] += d[i];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] *= dec_r;
+        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UB, rl * 64 + c4 * 16, u + 8 * c4);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UK, r * 64 + c4 * 16, u + 8 * c4);
-        }
+        for (int i = 0; i < 32; ++i) u[i] *= dec_r;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + OFF_UK, rl * 64 + c4 * 16, u + 8 * c4);
       }
       tc::fence_proxy_async();
       group_sync(kBarChain, kChainThreads);
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tmem + TM_O2,
-                       tc::smem_desc(sbase + OFF_PP + b * 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(sbase + OFF_UB + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_PU,
-                       kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tmem + TM_S, tc::smem_desc(stg + kk * 2048, 16384, 1024, tc::kLayoutSw128),
+        for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U): the next chunk waits on this
+          tc::mma_bf16(tmem + TM_S, tc::smem_desc(stg + ST_K + kk * 2048, kHalfBytes, 1024, tc::kLayoutSw128),
                        tc::smem_desc(sbase + OFF_UK + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_SU,
                        1);
         tc::mma_commit(&bars->mma_chain);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // O2 = P U in rows 64-127
+          tc::mma_bf16(tmem + TM_O2,
+                       tc::smem_desc(sbase + OFF_PP + b * 8192 - 8192 + kk * 32, 16, 1024,
+                                     tc::kLayoutSw128),
+                       tc::smem_desc(sbase + OFF_UB + kk * 1024, 4096, 512, tc::kLayoutSw64), ID_PU,
+                       kk > 0);
+        tc::mma_commit(&bars->mma_out);
       }
-      ok = group_wait(&bars->mma_chain, mma_phase & 1, kBarChain, kChainThreads);
-      ++mma_phase;
+      ok = group_wait(&bars->mma_chain, chain_phase & 1, kBarChain, kChainThreads);
+      ++chain_phase;
       if (!ok) break;
-      if (leader) {  // W, P, U~ and gates of buffer b, and the stage, are consumed
-        tc::mbar_arrive(&bars->chain_free[b]);
-        tc::mbar_arrive(&bars->stage_free[st]);
-      }
+      if (leader) tc::mbar_arrive(&bars->stage_free[st]);  // K, Q, -W of the stage consumed
       {
-        float o1[32], o2[32];
-        tc::tmem_ld32(tmem + lane_base + TM_O1, o1);
-        tc::tmem_ld32(tmem + lane_base + TM_O2, o2);
-        if (lane < 16 && r < nv) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
-          uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0 + r) * p.h_v + h) * (int64_t)p.d_v +
-                                                s * kDVS);
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint4 q4;
-            q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
-            q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
-            q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
-            q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
-            dst[c4] = q4;
-          }
-        }
         float sc[32];
         tc::tmem_ld32(tmem + lane_base + TM_S, sc);
         if (c == nchunks - 1) {
@@ -559,6 +615,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_proxy_async();
       group_sync(kBarChain, kChainThreads);
+      ok = group_wait(&bars->mma_out, out_phase & 1, kBarChain, kChainThreads);
+      ++out_phase;
+      if (!ok) break;
+      if (leader) tc::mbar_arrive(&bars->chain_free[b]);  // P, U~, gates of buffer b consumed
+      if (warp >= 2) {  // O = Gamma Q S^T + P U for rows r = lanes 64-127
+        float o1[32], o2[32];
+        tc::tmem_ld32(tmem + lane_base + TM_D0 + 32 * b, o1);
+        tc::tmem_ld32(tmem + lane_base + TM_O2, o2);
+        if (rl < nv) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0 + rl) * p.h_v + h) * (int64_t)p.d_v +
+                                                s * kDVS);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint4 q4;
+            q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
+            q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
+            q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
+            q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
+            dst[c4] = q4;
+          }
+        }
+      }
     }
   }
   if (!ok && (tid == 0 || tid == kChainThreads)) raise_error(p.err, kErrDeviceTimeout);
