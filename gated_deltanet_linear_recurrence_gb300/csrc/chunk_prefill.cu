@@ -41,7 +41,7 @@
 // Tensor-core products (bf16 operands, fp32 TMEM accumulators; an operand
 // written [X; Y] is an M=128 operand whose X rows are don't-care):
 //   prep:  G  = [Q;K] K^T          M=128 N=64  K=128  (rows 0-63: Q K^T, 64-127: K K^T)
-//          W  = [T b Gamma; .] K   M=128 N=128 K=64
+//          W  = (T b Gamma) K      M=64  N=128 K=64
 //          U~ = [T b; .] V_s       M=128 N=32  K=64
 //   chain: D  = [-W; Q] S_s^T      M=128 N=32  K=128  (rows 0-63: -W S^T, 64-127: Q S^T)
 //          S^T += K^T (e^{..} U)   M=128 N=32  K=64   (onto Gamma_n S^T)
@@ -77,7 +77,7 @@ constexpr int kChainThreads = 32 * kChainWarps;   // 128
 constexpr int kPrepThreads = 32 * kPrepWarps;     // 256
 constexpr int kThreads = kChainThreads + kPrepThreads + 32;  // + producer warp = 416
 constexpr int kProducerWarp = kChainWarps + kPrepWarps;      // warp 12
-constexpr uint32_t kBarChain = 1, kBarPrep = 2;               // named barrier ids
+constexpr uint32_t kBarChain = 1, kBarPrep = 2, kBarGate = 3;  // named barrier ids
 constexpr int kStages = 3;
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
@@ -120,7 +120,7 @@ constexpr uint32_t TM_G = 0, TM_W = 64, TM_U0 = 192, TM_D0 = 256, TM_O2 = 320, T
 
 // Instruction descriptors.
 constexpr uint32_t ID_G = tc::idesc_bf16_f32(128, 64, false, false);   // [Q;K] K^T
-constexpr uint32_t ID_W = tc::idesc_bf16_f32(128, 128, false, true);   // [TB;.] K
+constexpr uint32_t ID_W = tc::idesc_bf16_f32(64, 128, false, true);    // TB K
 constexpr uint32_t ID_UT = tc::idesc_bf16_f32(128, 32, false, true);   // [TA;.] V_s
 constexpr uint32_t ID_WQ = tc::idesc_bf16_f32(128, 32, false, true);   // [-W;Q] S_s^T
 constexpr uint32_t ID_SU = tc::idesc_bf16_f32(128, 32, true, true);    // K^T (decay U)
@@ -237,11 +237,18 @@ __device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt,
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
+      float av[16];
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        if (4 * i4 < r) {
+          const float4 v4 = *reinterpret_cast<const float4*>(MF + (o + r) * kLdM + o + 4 * i4);
+          av[4 * i4] = v4.x; av[4 * i4 + 1] = v4.y; av[4 * i4 + 2] = v4.z; av[4 * i4 + 3] = v4.w;
+        }
+      }
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll
       for (int i = 0; i < r; ++i) {
-        const float av = MF[(o + r) * kLdM + o + i];
-        if (i & 1) a1 = fmaf(av, x[i], a1); else a0 = fmaf(av, x[i], a0);
+        if (i & 1) a1 = fmaf(av[i], x[i], a1); else a0 = fmaf(av[i], x[i], a0);
       }
       x[r] = (r == cc) ? 1.f : ((r > cc) ? -(a0 + a1) : 0.f);
     }
@@ -366,22 +373,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pt = tid - kChainThreads;  // 0..255
     const int pw = pt >> 5;              // prep warp 0..7
     const int sp = pw & 3;               // TMEM subpartition of this warp
-    const bool leader = pt == 0;
+    const bool leader = pt == 0;         // arrives on the hand-off barriers
+    const bool issuer = pt == 64;        // issues the prep MMAs (not a gate warp)
     uint32_t mma_phase = 0;
+    // gates of the next chunk are loaded one iteration ahead (global latency)
+    auto load_gates = [&](int c, float& gv, float& bv) {
+      const int64_t tt = t_beg + (int64_t)c * kC + pt;
+      gv = 0.f;
+      bv = 0.f;
+      if (c < nchunks && pt < kC && tt < t_end) {
+        gv = p.g[tt * p.h_v + h];
+        bv = p.beta[tt * p.h_v + h];
+      }
+    };
+    float g_next, b_next;
+    load_gates(0, g_next, b_next);
     for (int c = 0; c < nchunks; ++c) {
       const int b = c & 1, st = c % kStages;
       const uint32_t stg = sbase + OFF_STAGE + st * kStageBytes;
       uint8_t* stg_ptr = smem + OFF_STAGE + st * kStageBytes;
       float* gate = reinterpret_cast<float*>(smem + OFF_GATE) + b * kGateFloats;
       float *gam = gate, *Gam = gate + 64, *bet = gate + 128, *dec = gate + 192;
-      const int64_t t0 = t_beg + (int64_t)c * kC;
-      const int nv = (int)((L - (int64_t)c * kC) < kC ? (L - (int64_t)c * kC) : kC);
 
-      float gr = 0.f, br = 0.f;
-      if (pt < nv) {
-        gr = p.g[(t0 + pt) * p.h_v + h];
-        br = p.beta[(t0 + pt) * p.h_v + h];
-      }
+      float gr = g_next, br = b_next;
+      load_gates(c + 1, g_next, b_next);
       // buffers b were last used by the chain for chunk c-2
       if (c >= 2) {
         ok = group_wait(&bars->chain_free[b], ((c >> 1) - 1) & 1, kBarPrep, kPrepThreads);
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = group_wait(&bars->tma_full[st], (c / kStages) & 1, kBarPrep, kPrepThreads);
       if (!ok) break;
-      if (leader) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
+      if (issuer) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t ko = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -408,16 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (pt == 31) MF[0] = x;  // scratch is free until the masks
         gr = x;
-      }
-      tc::named_sync(kBarPrep, kPrepThreads);
-      if (pt < 64) {
+        tc::named_sync(kBarGate, 64);
         if (pw == 1) gr += MF[0];
         gam[pt] = gr;
         Gam[pt] = tc::fast_exp(gr);
         bet[pt] = br;
+        tc::named_sync(kBarGate, 64);
+        dec[pt] = tc::fast_exp(gam[kC - 1] - gr);
       }
-      tc::named_sync(kBarPrep, kPrepThreads);
-      if (pt < 64) dec[pt] = tc::fast_exp(gam[kC - 1] - gam[pt]);
 
       // masks: P (bf16 operand) from rows 0-63, A (fp32, solve input) from rows 64-127
       ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
@@ -432,9 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = 32 * sp + lane;
           const float g_r = gam[r];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = i0 + e;
-            a[e] = (i <= r) ? tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+            const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int e = 4 * e4 + q, i = i0 + e;
+              a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] : 0.f;
+            }
           }
           uint8_t* pp = smem + OFF_PP + b * 8192;
 #pragma unroll
@@ -444,9 +462,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = 32 * (sp - 2) + lane;
           const float g_r = gam[r], b_r = bet[r];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = i0 + e;
-            MF[r * kLdM + i] = (i < r) ? b_r * tc::fast_exp(g_r - gam[i]) * a[e] : 0.f;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+            const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+            float o4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = i0 + 4 * e4 + q;
+              o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] : 0.f;
+            }
+            *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
+                make_float4(o4[0], o4[1], o4[2], o4[3]);
           }
         }
       }
@@ -454,26 +480,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       unit_lower_inverse(MF, YF, pt, lane);
 
-      {  // operands T diag(b Gamma) (prep threads 0-127) and T diag(b) (128-255)
-        const bool with_gamma = pt < 128;
-        const int r = (pt & 127) >> 1, half = pt & 1;
-        uint8_t* dst = smem + (with_gamma ? OFF_TB : OFF_TA);
+      {  // operands T diag(b Gamma) and T diag(b): thread = (row r, 16-column quarter)
+        const int r = pt >> 2, q = pt & 3;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const int i0 = 32 * half + 8 * c8;
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const int i0 = 16 * q + 8 * c8;
           const float4 m0 = *reinterpret_cast<const float4*>(MF + r * kLdM + i0);
           const float4 m1 = *reinterpret_cast<const float4*>(MF + r * kLdM + i0 + 4);
-          float x[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= bet[i0 + e] * (with_gamma ? Gam[i0 + e] : 1.f);
-          st_chunk<3>(dst, r * 128 + (4 * half + c8) * 16, x);
+          const float4 b0 = *reinterpret_cast<const float4*>(bet + i0);
+          const float4 b1 = *reinterpret_cast<const float4*>(bet + i0 + 4);
+          const float4 G0 = *reinterpret_cast<const float4*>(Gam + i0);
+          const float4 G1 = *reinterpret_cast<const float4*>(Gam + i0 + 4);
+          float xa[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
+                         m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
+          float xb[8] = {xa[0] * G0.x, xa[1] * G0.y, xa[2] * G0.z, xa[3] * G0.w,
+                         xa[4] * G1.x, xa[5] * G1.y, xa[6] * G1.z, xa[7] * G1.w};
+          st_chunk<3>(smem + OFF_TA, r * 128 + (2 * q + c8) * 16, xa);
+          st_chunk<3>(smem + OFF_TB, r * 128 + (2 * q + c8) * 16, xb);
         }
       }
       tc::fence_proxy_async();
       group_sync(kBarPrep, kPrepThreads);
 
-      // W = T b Gamma K and U~ = T b V on the tensor cores (rows 0-63 of M=128)
-      if (leader) {
+      // W = T b Gamma K and U~ = T b V on the tensor cores
+      if (issuer) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_bf16(tmem + TM_W, tc::smem_desc(sbase + OFF_TB + kk * 32, 16, 1024, tc::kLayoutSw128),
@@ -490,18 +520,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = group_wait(&bars->mma_prep, mma_phase & 1, kBarPrep, kPrepThreads);
       ++mma_phase;
       if (!ok) break;
-      if (sp < 2) {  // -W rows r = lanes 0-63 into the stage's W slots (K-major)
-        const int half = pw >> 2, r = 32 * sp + lane;
+      {  // -W into the stage's W slots (K-major); M=64 accumulator: row 16 sp + lane, lane < 16
+        const int half = pw >> 2, r = 16 * sp + lane;
         float w[32];
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           tc::tmem_ld32(tmem + lane_base + TM_W + 64 * half + 32 * q2, w);
+          if (lane < 16) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = -w[e];
+            for (int e = 0; e < 32; ++e) w[e] = -w[e];
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            st_chunk<3>(stg_ptr + half * kHalfBytes + ST_W, r * 128 + (4 * q2 + c8) * 16,
-                        w + 8 * c8);
+            for (int c8 = 0; c8 < 4; ++c8)
+              st_chunk<3>(stg_ptr + half * kHalfBytes + ST_W, r * 128 + (4 * q2 + c8) * 16,
+                          w + 8 * c8);
+          }
         }
       }
       tc::fence_proxy_async();
