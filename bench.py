@@ -200,6 +200,10 @@ def main():
     ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the token scan and the chunked prefill over sequence lengths "
+                         "(one sequence, 16 key / 32 value heads of 128, bf16) and print the "
+                         "crossover table as JSON lines")
     ap.add_argument("--kernel-only", choices=["prefill", "decode_b256"], default=None,
                     help="run only this kernel's workload (warmup + steps launches, no JSON); "
                          "for profiler captures")
@@ -210,6 +214,8 @@ def main():
         return run_reference(args)
     if args.kernel_only:
         return run_kernel_only(args)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist
@@ -443,6 +449,42 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
                                   "tok_s": 1 / (ms / 1e3),
                                   "l2": "flushed between steps; 30 calls in one CUDA graph"}
     return out
+
+
+def run_sweep(args):
+    """Scan vs chunked prefill time over sequence lengths (L2 flushed before each call)."""
+    import torch
+    from gated_deltanet_linear_recurrence_gb300 import gdn_prefill, gdn_stream_status, inputs
+
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    lengths = [16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 65536, 131072]
+    rows = []
+    for T in lengths:
+        d = inputs.make_prefill([T], 16, 32, 128, 128, "bf16", seed=T)
+        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        res = {"T": T}
+        for algo in ("scan", "chunked"):
+            reps = 3 if (algo == "scan" and T >= 16384) else 7
+            ts = []
+            for i in range(reps + 2):
+                flush_buf.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                            algo=algo)
+                b.record()
+                torch.cuda.synchronize()
+                if i >= 2:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            assert gdn_stream_status() == "GDN_OK"
+            res[algo + "_us"] = statistics.median(ts)
+        res["chunked_tok_s"] = T / (res["chunked_us"] / 1e6)
+        res["scan_tok_s"] = T / (res["scan_us"] / 1e6)
+        rows.append(res)
+        print(json.dumps(res), flush=True)
+    cross = next((r["T"] for r in rows if r["chunked_us"] < r["scan_us"]), None)
+    print(json.dumps({"crossover_tokens": cross}), flush=True)
 
 
 def run_kernel_only(args):

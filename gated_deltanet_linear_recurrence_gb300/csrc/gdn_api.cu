@@ -42,11 +42,18 @@ gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
   return GDN_OK;
 }
 
-// Measured crossover (sequence length from which the chunked evaluation is
-// faster than the token scan) for bf16 inputs, by head dimension.
+// Crossover: the sequence length from which the chunked evaluation is faster
+// than the token scan.  Measured on GB300 (bench.py --sweep: one sequence,
+// 16 key / 32 value heads of 128, bf16; L2 flushed before each call): the
+// chunked kernel was faster at every measured length from 16 tokens up
+// (12.9 vs 19.1 us at 16 tokens, 12x faster from 1K tokens), so sequences
+// shorter than 16 tokens use the scan.  Shapes the chunked kernel does not
+// cover (d_k != 128, d_v not a multiple of 32, fp32 inputs) always scan.
+constexpr int32_t kCrossoverTokens = 16;
+
 int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return INT32_MAX;
-  return 64;
+  return kCrossoverTokens;
 }
 
 }  // namespace
