@@ -34,6 +34,30 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NUM_SMS_GB300 = 152
 FP32_LANES_PER_SM = 128
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of each kernel (summaries under profiles/), valid only while the
+# kernel's sources hash to the recorded value.
+NCU_TRAFFIC = {
+    "chunk_prefill": {"files": ["chunk_prefill.cu", "tc.cuh", "rows.cuh", "params.h"],
+                      "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
+                      "profile": "profiles/chunk_prefill_t4096.md"},
+    "decode_step": {"files": ["decode_step.cu", "rows.cuh", "params.h"],
+                    "sha256_16": "bdc6d4c3a147886a", "bytes": 541_162_496 + 479_516_672,
+                    "profile": "profiles/decode_step_b256.md"},
+}
+
+
+def ncu_traffic(kernel):
+    """Recorded DRAM bytes per launch, or None if the kernel changed since the capture."""
+    import hashlib
+
+    rec = NCU_TRAFFIC[kernel]
+    m = hashlib.sha256()
+    for f in rec["files"]:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_recurrence_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return rec["bytes"] if m.hexdigest()[:16] == rec["sha256_16"] else None
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -293,7 +317,8 @@ def main():
         flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": ncu_traffic("chunk_prefill"),
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
                 "algorithmic_flop_per_launch": flop}
     else:
@@ -404,7 +429,7 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
                           "frac_of_8tbs_nominal": gbs / 8000.0,
                           "tok_s": w["batch"] / (ms / 1e3), "l2": "state 1 GiB > L2"}
     out["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                       "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                       "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic("decode_step"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
     del y, o, dd
 
