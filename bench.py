@@ -38,6 +38,10 @@ FP32_LANES_PER_SM = 128
 # ncu capture of each kernel (summaries under profiles/), valid only while the
 # kernel's sources hash to the recorded value.
 NCU_TRAFFIC = {
+    "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh",
+                              "params.h"],
+                    "sha256_16": "unmeasured", "bytes": None,
+                    "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "tc.cuh", "rows.cuh", "params.h"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
@@ -310,15 +314,20 @@ def main():
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1e3)
-    launches_per_step = 1
+    # chunked with workspace: plan + prepare + chain kernels; fused or scan: one kernel
+    launches_per_step = 3 if (algo_used == "chunked" and ws_n > 0) else 1
 
     # roofline of the prefill kernel (one launch per step)
     if algo_used == "chunked":
         flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
+        split = ws_n > 0
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": ncu_traffic("chunk_prefill"),
+                "traffic": ncu_traffic("chunk_split" if split else "chunk_prefill"),
+                "scope": ("the whole gdn_prefill call: chunk_plan + chunk_prepare + chunk_chain "
+                          "kernels (one algorithm split in two; shares in profiles/)") if split
+                         else "the fused chunk_prefill kernel",
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
                 "algorithmic_flop_per_launch": flop}
     else:
@@ -483,13 +492,16 @@ def run_sweep(args):
 
     dev = torch.device("cuda", 0)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    lengths = [16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 65536, 131072]
+    lengths = [8, 16, 32, 64, 128, 256, 384, 512, 768, 1024, 2048, 4096, 8192, 16384, 65536,
+               131072]
     rows = []
     for T in lengths:
         d = inputs.make_prefill([T], 16, 32, 128, 128, "bf16", seed=T)
         x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
         res = {"T": T}
-        for algo in ("scan", "chunked"):
+        # chunked = two kernels through a workspace; chunked_fused = one kernel, none
+        for name, algo in (("scan", "scan"), ("chunked", "chunked_split"),
+                           ("chunked_fused", "chunked_fused")):
             reps = 3 if (algo == "scan" and T >= 16384) else 7
             ts = []
             for i in range(reps + 2):
@@ -503,13 +515,16 @@ def run_sweep(args):
                 if i >= 2:
                     ts.append(a.elapsed_time(b) * 1e3)
             assert gdn_stream_status() == "GDN_OK"
-            res[algo + "_us"] = statistics.median(ts)
+            res[name + "_us"] = statistics.median(ts)
         res["chunked_tok_s"] = T / (res["chunked_us"] / 1e6)
+        res["chunked_fused_tok_s"] = T / (res["chunked_fused_us"] / 1e6)
         res["scan_tok_s"] = T / (res["scan_us"] / 1e6)
         rows.append(res)
         print(json.dumps(res), flush=True)
-    cross = next((r["T"] for r in rows if r["chunked_us"] < r["scan_us"]), None)
-    print(json.dumps({"crossover_tokens": cross}), flush=True)
+    cross = next((r["T"] for r in rows
+                  if min(r["chunked_us"], r["chunked_fused_us"]) < r["scan_us"]), None)
+    split = next((r["T"] for r in rows if r["chunked_us"] < r["chunked_fused_us"]), None)
+    print(json.dumps({"crossover_tokens": cross, "split_from_tokens": split}), flush=True)
 
 
 def run_kernel_only(args):

@@ -17,7 +17,7 @@ STATUS_NAMES = {
     9: "GDN_ERR_CUDA",
 }
 GDN_F32, GDN_BF16 = 0, 1
-ALGOS = {"auto": 0, "scan": 1, "chunked": 2}
+ALGOS = {"auto": 0, "scan": 1, "chunked": 2, "chunked_fused": 3, "chunked_split": 4}
 
 # Exported symbols, with ctypes signatures: (restype, argtypes)
 _vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,

@@ -1,0 +1,729 @@
+// chunk_split.cu — chunked (WY/UT) prefill as two kernels that meet in a
+// caller-provided workspace.
+//
+// The block form of the recurrence (page "Optimizing on-device inference for
+// Apple Silicon", section "Qwen creates three distinct workload shapes") splits
+// into work that does not depend on the state — per chunk of 64 tokens and
+// value head: gates, the Q K^T / K K^T masks, the triangular solve
+// T = (I + A)^{-1}, W = T diag(b Gamma) K — and the sequential state pass.
+// chunk_prepare_kernel does the first part once per (chunk, value head), spread
+// over every SM, and writes a "package" per item to the workspace, already in
+// the swizzled shared-memory layout the tensor cores read:
+//
+//   [ -W half 0 | -W half 1 ]  bf16 [r][j], K-major SWIZZLE_128B, 2 x 8 KB
+//   [ P ]                      bf16 [r][i], 8 KB   (e^{gamma_r - gamma_i} q_r.k_i, i <= r)
+//   [ T b ]                    bf16 [r][i], 8 KB   (T diag(beta))
+//   [ gates ]                  fp32 Gamma[64], decay[64] (e^{gamma_n - gamma_r}), Gamma_n
+//
+// chunk_chain_kernel walks each (sequence, value head, 32-row slice of d_v) in
+// chunk order with the fp32 state in TMEM, bulk-copying the packages into a
+// 3-stage ring next to the TMA'd Q, K and V slice:
+//   U~ = (T b) V_s,  D = [-W; Q] S^T,  U = U~ + D_top,
+//   S^T <- Gamma_n S^T + K^T (decay U),  O = Gamma D_bottom + P U.
+// Only D, U and the state update are on the chunk-to-chunk critical path: U~
+// of chunk c+1 is issued as soon as its stage has landed (it runs while chunk
+// c's U is formed), P U of chunk c runs while chunk c's state is staged for the
+// next chunk, and chunk c's output is written while chunk c+1's D product runs.
+// chunk_plan_kernel computes each sequence's first package index (an exclusive
+// prefix sum of its chunk count) into the workspace header and records an
+// inconsistent cu_seqlens in the error word.
+//
+// Compared with the single fused kernel (chunk_prefill.cu) the key-side work is
+// done once per head instead of once per slice, and the chain's SM no longer
+// shares its tensor pipe and shared memory with it.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "chunk_common.cuh"
+#include "params.h"
+#include "rows.cuh"
+#include "tc.cuh"
+
+namespace gdn {
+
+// Workspace layout (shared with the host-side size computation).
+constexpr uint32_t kPkgW = 0, kPkgP = 16384, kPkgTA = 24576, kPkgGates = 32768;
+constexpr uint32_t kPkgBytes = 33792;  // 33 KB, a multiple of 1024 (swizzle phase)
+
+size_t split_header_bytes(int32_t num_seqs) {
+  return ((size_t)(num_seqs + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
+}
+size_t split_max_items(int32_t num_seqs, int64_t total_tokens, int32_t h_v) {
+  // sum_n ceil(L_n / 64) <= T / 64 + N
+  return ((size_t)(total_tokens / chunk::kC) + (size_t)num_seqs + 1) * (size_t)h_v;
+}
+
+namespace {
+
+using namespace chunk;
+
+struct SplitParams {
+  const float* g;
+  const float* beta;
+  const float* state_in;
+  float* state_out;
+  __nv_bfloat16* o;
+  const int32_t* cu;
+  int32_t num_seqs;
+  int64_t total_tokens;
+  int32_t h_k, h_v, d_v;
+  float scale;
+  int32_t min_len;
+  int32_t* chunk_base;  // [N+1] in the workspace header
+  uint8_t* packages;    // items x kPkgBytes
+  int64_t max_items;
+  int* err;
+};
+
+__device__ __forceinline__ bool seq_range(const SplitParams& p, int n, int64_t& t0, int64_t& t1) {
+  t0 = p.cu[n];
+  t1 = p.cu[n + 1];
+  return !(t0 < 0 || t1 < t0 || t1 > p.total_tokens || (n == 0 && t0 != 0) ||
+           (n == p.num_seqs - 1 && t1 != p.total_tokens));
+}
+
+// ------------------------------------------------------------------ plan
+__global__ void __launch_bounds__(256) chunk_plan_kernel(const SplitParams p) {
+  __shared__ int32_t warp_sums[8];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < p.num_seqs; base += 256) {
+    const int n = base + threadIdx.x;
+    int32_t cnt = 0;
+    if (n < p.num_seqs) {
+      int64_t t0, t1;
+      if (seq_range(p, n, t0, t1)) {
+        const int64_t L = t1 - t0;
+        if (L >= p.min_len) cnt = (int32_t)((L + kC - 1) / kC);
+      } else {
+        raise_error(p.err, kErrBadCuSeqlens);
+      }
+    }
+    // block-wide exclusive scan of cnt
+    int32_t x = cnt;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(kFullMask, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    int32_t wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += warp_sums[w];
+    const int32_t incl = carry + wbase + x;
+    if (n < p.num_seqs) p.chunk_base[n] = incl - cnt;
+    __syncthreads();
+    if (threadIdx.x == 255) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.chunk_base[p.num_seqs] = carry;
+}
+
+// ------------------------------------------------------------------ prepare
+constexpr int kPrepThreads = 256;
+constexpr uint32_t kBarAll = 1, kBarGateP = 2;
+// shared memory of the prepare kernel
+constexpr uint32_t PP_KQ = 0;                      // per d_k half: [Q 8K][K 8K]
+constexpr uint32_t PP_TB = 32768;                  // T diag(b Gamma) bf16, SW128 (solve scratch first)
+constexpr uint32_t PP_MF = PP_TB + 8192;           // A, then T: fp32 [64][kLdM]
+constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;  // gamma, Gamma, beta, decay
+constexpr uint32_t PP_MISC = PP_GATE + 4 * 64 * 4;
+constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
+constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W (0-127)
+constexpr uint32_t IDP_G = tc::idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t IDP_W = tc::idesc_bf16_f32(64, 128, false, true);
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31, sp = pw & 3;
+  const int64_t item = blockIdx.x;
+  const int64_t cid = item / p.h_v;
+  const int h = (int)(item % p.h_v);
+  const int32_t total_chunks = p.chunk_base[p.num_seqs];
+  if (cid >= total_chunks) return;
+  // the sequence owning chunk cid: last n with chunk_base[n] <= cid (skipping empty ones)
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.chunk_base[mid] <= cid) lo = mid; else hi = mid - 1;
+  }
+  const int n = lo;
+  const int c = (int)(cid - p.chunk_base[n]);
+  const int64_t t_beg = p.cu[n], t_end = p.cu[n + 1];
+  const int64_t t0 = t_beg + (int64_t)c * kC;
+  const int hk = h / (p.h_v / p.h_k);
+  uint8_t* pkg = p.packages + item * (int64_t)kPkgBytes;
+
+  float* MF = reinterpret_cast<float*>(smem + PP_MF);
+  float* YF = reinterpret_cast<float*>(smem + PP_TB);
+  float* gam = reinterpret_cast<float*>(smem + PP_GATE);
+  float *Gam = gam + 64, *bet = gam + 128, *dec = gam + 192;
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);
+  uint64_t* bar_mma = bar_tma + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 2);
+  const uint32_t sbase = tc::smem_u32(smem);
+
+  if (pw == 0) {
+    tc::tmem_alloc(tmem_slot, kPrepTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (pt == 0) {
+    tc::mbar_init(bar_tma, 1);
+    tc::mbar_init(bar_mma, 1);
+    tc::fence_mbar_init();
+    tc::mbar_arrive_expect_tx(bar_tma, 32768);
+    const int32_t y = static_cast<int32_t>(t0);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::tma_load_2d(smem + PP_KQ + kb * 16384, &tm_q, hk * kDK + 64 * kb, y, bar_tma);
+      tc::tma_load_2d(smem + PP_KQ + kb * 16384 + 8192, &tm_k, hk * kDK + 64 * kb, y, bar_tma);
+    }
+  }
+  float gr = 0.f, br = 0.f;
+  if (pt < kC && t0 + pt < t_end) {
+    gr = p.g[(t0 + pt) * p.h_v + h];
+    br = p.beta[(t0 + pt) * p.h_v + h];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+  bool ok = tc::mbar_wait(bar_tma, 0);
+  tc::fence_after_sync();
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  if (ok) {
+    if (pt == 64) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+        tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_KQ + ko, 16, 1024, tc::kLayoutSw128),
+                     tc::smem_desc(sbase + PP_KQ + ko + 8192, 16, 1024, tc::kLayoutSw128), IDP_G,
+                     kk > 0);
+      }
+      tc::mma_commit(bar_mma);
+    }
+    if (pt < 64) {  // gates: inclusive scan of g over the chunk
+      float x = gr;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(kFullMask, x, off);
+        if (lane >= off) x += y;
+      }
+      if (pt == 31) MF[0] = x;
+      tc::named_sync(kBarGateP, 64);
+      if (pw == 1) x += MF[0];
+      gam[pt] = x;
+      Gam[pt] = tc::fast_exp(x);
+      bet[pt] = br;
+      tc::named_sync(kBarGateP, 64);
+      dec[pt] = tc::fast_exp(gam[kC - 1] - x);
+      float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
+      gout[pt] = Gam[pt];
+      gout[64 + pt] = dec[pt];
+      if (pt == 0) gout[128] = Gam[kC - 1];
+    }
+    ok = tc::mbar_wait(bar_mma, 0);
+    tc::fence_after_sync();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  }
+  if (ok) {
+    // masks: P rows (subpartitions 0,1) to the package, A rows (2,3) to MF
+    const int half = pw >> 2, i0 = 32 * half;
+    float a[32];
+    tc::tmem_ld32(tmem + lane_base + 32 * half, a);
+    if (sp < 2) {
+      const int r = 32 * sp + lane;
+      const float g_r = gam[r];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+        const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = 4 * e4 + q, i = i0 + e;
+          a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(pkg + kPkgP, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+    } else {
+      const int r = 32 * (sp - 2) + lane;
+      const float g_r = gam[r], b_r = bet[r];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+        const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+        float o4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = i0 + 4 * e4 + q;
+          o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] : 0.f;
+        }
+        *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
+            make_float4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+    tc::fence_before_sync();
+    tc::named_sync(kBarAll, kPrepThreads);
+    tc::fence_after_sync();
+
+    unit_lower_inverse<kBarAll, kPrepThreads>(MF, YF, pt, lane);
+
+    {  // T diag(b Gamma) to shared memory (W operand), T diag(b) to the package
+      const int r = pt >> 2, q = pt & 3;
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const int ii = 16 * q + 8 * c8;
+        const float4 m0 = *reinterpret_cast<const float4*>(MF + r * kLdM + ii);
+        const float4 m1 = *reinterpret_cast<const float4*>(MF + r * kLdM + ii + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(bet + ii);
+        const float4 b1 = *reinterpret_cast<const float4*>(bet + ii + 4);
+        const float4 G0 = *reinterpret_cast<const float4*>(Gam + ii);
+        const float4 G1 = *reinterpret_cast<const float4*>(Gam + ii + 4);
+        float xa[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
+                       m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
+        float xb[8] = {xa[0] * G0.x, xa[1] * G0.y, xa[2] * G0.z, xa[3] * G0.w,
+                       xa[4] * G1.x, xa[5] * G1.y, xa[6] * G1.z, xa[7] * G1.w};
+        st_chunk<3>(pkg + kPkgTA, r * 128 + (2 * q + c8) * 16, xa);
+        st_chunk<3>(smem + PP_TB, r * 128 + (2 * q + c8) * 16, xb);
+      }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    tc::named_sync(kBarAll, kPrepThreads);
+    tc::fence_after_sync();
+    if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (overwrites G's columns)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_TB + kk * 32, 16, 1024, tc::kLayoutSw128),
+                     tc::smem_desc(sbase + PP_KQ + 8192 + kk * 2048, 16384, 1024, tc::kLayoutSw128),
+                     IDP_W, kk > 0);
+      tc::mma_commit(bar_mma);
+    }
+    ok = tc::mbar_wait(bar_mma, 1);
+    tc::fence_after_sync();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (ok) {  // -W (M=64 accumulator: row 16 sp + lane on lanes 0-15) to the package
+      const int r = 16 * sp + lane;
+      float w[32];
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        tc::tmem_ld32(tmem + lane_base + 64 * half + 32 * q2, w);
+        if (lane < 16) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = -w[e];
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_chunk<3>(pkg + kPkgW + half * 8192, r * 128 + (4 * q2 + c8) * 16, w + 8 * c8);
+        }
+      }
+    }
+  }
+  if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (pw == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// ------------------------------------------------------------------ chain
+constexpr int kChainThreads = 128;
+constexpr int kChainKernelThreads = kChainThreads + 32;  // + producer warp
+constexpr int kProducerWarp = 4;
+constexpr uint32_t kBarChain = 1, kBarU = 2, kBarO = 3;  // all 4 warps; warps 0-1; warps 2-3
+constexpr int kStages = 3;
+// Main stage: per d_k half kb [-W | Q | K] (8 KB each; [-W; Q] is one 128-row
+// operand), then T b (8 KB) and the V slice (4 KB); released once the chunk's
+// state update is done.  Tail stage: P (8 KB) and the gates, released after the
+// chunk's output (one chunk later).  The 64 rows after T b and before each P
+// are valid shared memory, as M=128 operands whose other half is never read.
+constexpr uint32_t kHalf = 24576;
+constexpr uint32_t SC_W = 0, SC_Q = 8192, SC_K = 16384, SC_TA = 2 * kHalf, SC_V = SC_TA + 8192;
+constexpr uint32_t kMain = SC_V + 4096;                                    // 61440
+constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + 8192 + 4096;
+static_assert(kMainTx == kMain, "every main-stage byte arrives by TMA or bulk copy");
+constexpr uint32_t TL_P = 0, TL_G = 8192;
+constexpr uint32_t kTail = 9216;
+constexpr uint32_t kTailTx = 8192 + 1024;
+constexpr uint32_t CC_TAIL = kStages * kMain;
+constexpr uint32_t CC_SS = CC_TAIL + kStages * kTail;    // S slice bf16 [j][i], SW64, 8 KB
+constexpr uint32_t CC_UB = CC_SS + 8192;                 // U bf16 [r][i], SW64
+constexpr uint32_t CC_UK = CC_UB + 4096;                 // decayed U bf16 [r][i], SW64
+constexpr uint32_t CC_MISC = CC_UK + 4096;
+constexpr uint32_t kChainSmem = CC_MISC + 256 + 1024;
+static_assert(kChainSmem <= 227 * 1024, "shared memory budget");
+static_assert(kMain % 1024 == 0 && kTail % 1024 == 0 && CC_TAIL % 1024 == 0 &&
+                  CC_SS % 1024 == 0 && SC_TA % 1024 == 0 && SC_V % 512 == 0,
+              "swizzled operands need 1024 / 512 byte alignment");
+constexpr uint32_t kChainTmemCols = 256;
+constexpr uint32_t TC_U0 = 0, TC_D0 = 64, TC_O0 = 128, TC_S = 192;  // U~, D, P U double-buffered
+constexpr uint32_t IDC_UT = tc::idesc_bf16_f32(128, 32, false, true);  // [T b; .] V_s
+constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, 32, false, true);  // [-W; Q] S^T
+constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, 32, true, true);   // K^T (decay U)
+constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, 32, false, true);  // [.; P] U (rows 64-127)
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kChainKernelThreads, 1)
+    chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = p.d_v / kDVS;
+  const int s = blockIdx.x % ns;
+  const int h = (blockIdx.x / ns) % p.h_v;
+  const int n = blockIdx.x / (ns * p.h_v);
+  const int hk = h / (p.h_v / p.h_k);
+  int64_t t_beg, t_end;
+  if (!seq_range(p, n, t_beg, t_end)) return;  // reported by the plan kernel
+  const int64_t L = t_end - t_beg;
+  if (L < p.min_len) return;  // the token scan owns this sequence
+  const int nchunks = (int)((L + kC - 1) / kC);
+  const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
+  const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CC_MISC);  // main stages
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;                              // tail stages
+  uint64_t* tempty = tfull + kStages;
+  uint64_t* bar_d = tempty + kStages;  // [-W; Q] S^T (and every earlier MMA)
+  uint64_t* bar_s = bar_d + 1;         // state update
+  uint64_t* bar_o = bar_s + 1;         // P U, one barrier per chunk parity
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kChainTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 1);
+    }
+    tc::mbar_init(bar_d, 1);
+    tc::mbar_init(bar_s, 1);
+    tc::mbar_init(&bar_o[0], 1);
+    tc::mbar_init(&bar_o[1], 1);
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  bool ok = true;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(&tm_v);
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kStages;
+        const uint8_t* pkg = p.packages + (first_item + (int64_t)c * p.h_v) * kPkgBytes;
+        if (c >= kStages && !tc::mbar_wait(&empty[st], ((c / kStages) - 1) & 1)) {
+          raise_error(p.err, kErrDeviceTimeout);
+          break;
+        }
+        uint8_t* dst = smem + st * kMain;
+        const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
+        uint64_t* fb = &full[st];
+        tc::mbar_arrive_expect_tx(fb, kMainTx);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          tc::tma_load_2d(dst + kb * kHalf + SC_Q, &tm_q, hk * kDK + 64 * kb, y, fb);
+          tc::tma_load_2d(dst + kb * kHalf + SC_K, &tm_k, hk * kDK + 64 * kb, y, fb);
+          bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
+        }
+        bulk_g2s(dst + SC_TA, pkg + kPkgTA, 8192, fb);
+        tc::tma_load_2d(dst + SC_V, &tm_v, h * p.d_v + s * kDVS, y, fb);
+        if (c >= kStages && !tc::mbar_wait(&tempty[st], ((c / kStages) - 1) & 1)) {
+          raise_error(p.err, kErrDeviceTimeout);
+          break;
+        }
+        uint8_t* tl = smem + CC_TAIL + st * kTail;
+        tc::mbar_arrive_expect_tx(&tfull[st], kTailTx);
+        bulk_g2s(tl + TL_P, pkg + kPkgP, 8192, &tfull[st]);
+        bulk_g2s(tl + TL_G, pkg + kPkgGates, 1024, &tfull[st]);
+      }
+    }
+  } else {
+    // Chain warps.  Warps 0-1 (TMEM lanes 0-63) form U; warps 2-3 (lanes 64-127)
+    // write the previous chunk's output meanwhile; all four stage the state.
+    const bool leader = tid == 0;
+    uint32_t ph_d = 0, ph_s = 0;
+    const uint32_t ss = sbase + CC_SS;
+    const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
+    int u_issued = -1;                       // last chunk whose U~ product is issued (leader)
+    auto issue_u = [&](int cu_) {  // U~ = (T b) V_s of chunk cu_ into TC_U0 + 32 (cu_ & 1)
+      const uint32_t stg = sbase + (cu_ % kStages) * kMain;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(tmem + TC_U0 + 32 * (cu_ & 1),
+                     tc::smem_desc(stg + SC_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
+                     tc::smem_desc(stg + SC_V + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_UT,
+                     kk > 0);
+      u_issued = cu_;
+    };
+    // Output of chunk cp (warps 2-3): O = Gamma Q S^T + P U for rows r = lanes
+    // 64-127, then release its tail stage.
+    auto finish_output = [&](int cp) {
+      const int stp = cp % kStages;
+      const float* gp = reinterpret_cast<const float*>(smem + CC_TAIL + stp * kTail + TL_G);
+      // chunk cp + 2 commits to the same barrier only after this wait (the
+      // chain barrier of chunk cp + 1 orders them), so the parity is unambiguous
+      ok = tc::mbar_wait(&bar_o[cp & 1], (cp >> 1) & 1) && ok;
+      tc::fence_after_sync();
+      const int64_t t0p = t_beg + (int64_t)cp * kC;
+      const int nvp = (int)((L - (int64_t)cp * kC) < kC ? (L - (int64_t)cp * kC) : kC);
+      float o1[32], o2[32];
+      tc::tmem_ld32(tmem + lane_base + TC_D0 + 32 * (cp & 1), o1);
+      tc::tmem_ld32(tmem + lane_base + TC_O0 + 32 * (cp & 1), o2);
+      if (rl < nvp) {
+        const float Gam_r = gp[rl];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0p + rl) * p.h_v + h) * (int64_t)p.d_v +
+                                              s * kDVS);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint4 q4;
+          q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
+          q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
+          q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
+          q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
+          dst[c4] = q4;
+        }
+      }
+      tc::fence_before_sync();
+      tc::named_sync(kBarO, 64);
+      if (tid == 64) tc::mbar_arrive(&tempty[stp]);
+    };
+    // S (fp32, thread j holds column j of the slice) -> bf16 operand copy, then
+    // Gamma_n of chunk cn applied in TMEM (the update MMA accumulates onto it).
+    auto stage_state = [&](float (&sc)[32], int cn) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_SS, tid * 64 + c4 * 16, sc + 8 * c4);
+      const int stn = cn % kStages;
+      ok = tc::mbar_wait(&tfull[stn], (cn / kStages) & 1) && ok;
+      const float Gam_n = reinterpret_cast<const float*>(smem + CC_TAIL + stn * kTail + TL_G)[128];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
+      tc::tmem_st32(tmem + lane_base + TC_S, sc);
+    };
+    {  // initial state
+      float sc[32];
+#pragma unroll
+      for (int i = 0; i < kDVS; ++i)
+        sc[i] = p.state_in ? p.state_in[(srow0 + i) * kDK + tid] : 0.f;
+      if (nchunks == 0) {
+#pragma unroll
+        for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+      } else {
+        stage_state(sc, 0);
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      ok = tc::named_sync_and(kBarChain, kChainThreads, ok);
+      tc::fence_after_sync();
+    }
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c % kStages;
+      const uint32_t stg = sbase + st * kMain;
+      const float* gates = reinterpret_cast<const float*>(smem + CC_TAIL + st * kTail + TL_G);
+      if (leader) {
+        ok = tc::mbar_wait(&full[st], (c / kStages) & 1) && ok;
+        tc::fence_after_sync();
+        if (u_issued < c) issue_u(c);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // D = [-W; Q] S_s^T
+          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TC_D0 + 32 * (c & 1),
+                       tc::smem_desc(stg + ko + SC_W, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_WQ, kk > 0);
+        }
+        tc::mma_commit(bar_d);
+      }
+      if (warp < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
+        ok = tc::mbar_wait(bar_d, ph_d & 1) && ok;
+        tc::fence_after_sync();
+        const float dec_r = gates[64 + rl];
+        float u[32], d[32];
+        tc::tmem_ld32(tmem + lane_base + TC_U0 + 32 * (c & 1), u);
+        tc::tmem_ld32(tmem + lane_base + TC_D0 + 32 * (c & 1), d);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] += d[i];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_UB, rl * 64 + c4 * 16, u + 8 * c4);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] *= dec_r;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_UK, rl * 64 + c4 * 16, u + 8 * c4);
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        tc::named_sync(kBarU, 64);
+        tc::fence_after_sync();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U): the next chunk waits on this
+            tc::mma_bf16(tmem + TC_S,
+                         tc::smem_desc(stg + SC_K + kk * 2048, kHalf, 1024, tc::kLayoutSw128),
+                         tc::smem_desc(sbase + CC_UK + kk * 1024, 4096, 512, tc::kLayoutSw64),
+                         IDC_SU, 1);
+          tc::mma_commit(bar_s);
+          const uint32_t tl = sbase + CC_TAIL + st * kTail;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127) while the state is staged
+            tc::mma_bf16(tmem + TC_O0 + 32 * (c & 1),
+                         tc::smem_desc(tl + TL_P - 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
+                         tc::smem_desc(sbase + CC_UB + kk * 1024, 4096, 512, tc::kLayoutSw64),
+                         IDC_PU, kk > 0);
+          tc::mma_commit(&bar_o[c & 1]);
+          // the next chunk's U~, if its stage has landed
+          if (c + 1 < nchunks &&
+              tc::mbar_try_wait(&full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
+            tc::fence_after_sync();
+            issue_u(c + 1);
+          }
+        }
+      } else if (c > 0) {
+        finish_output(c - 1);  // warps 2-3, while U is formed
+      }
+      ++ph_d;
+      ok = tc::mbar_wait(bar_s, ph_s & 1) && ok;
+      tc::fence_after_sync();
+      ++ph_s;
+      if (leader) tc::mbar_arrive(&empty[st]);  // -W, Q, K, T b and V of the stage consumed
+      {
+        float sc[32];
+        tc::tmem_ld32(tmem + lane_base + TC_S, sc);
+        if (c == nchunks - 1) {
+#pragma unroll
+          for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+        } else {
+          stage_state(sc, c + 1);
+        }
+      }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      ok = tc::named_sync_and(kBarChain, kChainThreads, ok);
+      tc::fence_after_sync();
+    }
+    if (ok && nchunks > 0 && warp >= 2) finish_output(nchunks - 1);  // the last chunk's output
+  }
+  if (!ok && tid == 0) raise_error(p.err, kErrDeviceTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, kChainTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t split_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v) {
+  return split_header_bytes(num_seqs) + split_max_items(num_seqs, total_tokens, h_v) * kPkgBytes;
+}
+
+cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  const uint64_t rows = a.total_tokens > 0 ? (uint64_t)a.total_tokens : 1;
+  const void* qp = a.total_tokens > 0 ? a.q : a.state_out;
+  const void* kp = a.total_tokens > 0 ? a.k : a.state_out;
+  const void* vp = a.total_tokens > 0 ? a.v : a.state_out;
+  if (!encode_map(&mq, qp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, kDVS, kC, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(chunk_prepare_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(chunk_chain_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  SplitParams p;
+  p.g = a.g;
+  p.beta = a.beta;
+  p.state_in = a.state_in;
+  p.state_out = a.state_out;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.cu = a.cu_seqlens;
+  p.num_seqs = a.num_seqs;
+  p.total_tokens = a.total_tokens;
+  p.h_k = a.h_k;
+  p.h_v = a.h_v;
+  p.d_v = a.d_v;
+  p.scale = a.scale;
+  p.min_len = a.min_chunk_len;
+  p.chunk_base = static_cast<int32_t*>(workspace);
+  p.packages = static_cast<uint8_t*>(workspace) + split_header_bytes(a.num_seqs);
+  p.max_items = (int64_t)split_max_items(a.num_seqs, a.total_tokens, a.h_v);
+  p.err = a.err;
+  chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.max_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  chunk_prepare_kernel<<<(unsigned)p.max_items, kPrepThreads, kPrepSmem, stream>>>(mq, mk, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t grid = (int64_t)a.num_seqs * a.h_v * (a.d_v / kDVS);
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  chunk_chain_kernel<<<(unsigned)grid, kChainKernelThreads, kChainSmem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -45,11 +45,22 @@ gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
 // Crossover: the sequence length from which the chunked evaluation is faster
 // than the token scan.  Measured on GB300 (bench.py --sweep: one sequence,
 // 16 key / 32 value heads of 128, bf16; L2 flushed before each call): the
-// chunked kernel was faster at every measured length from 16 tokens up
-// (12.9 vs 19.1 us at 16 tokens, 12x faster from 1K tokens), so sequences
-// shorter than 16 tokens use the scan.  Shapes the chunked kernel does not
-// cover (d_k != 128, d_v not a multiple of 32, fp32 inputs) always scan.
+// fused chunked kernel ties the scan at 8 tokens (13.0 vs 12.9 us) and is
+// faster from 16 tokens up (13.0 vs 19.1 us), so sequences shorter than 16
+// tokens use the scan.  Shapes the chunked kernels do not cover (d_k != 128,
+// d_v not a multiple of 32, fp32 inputs) always scan.
 constexpr int32_t kCrossoverTokens = 16;
+
+// Fused vs two-kernel chunked evaluation.  Same sweep: the fused kernel is
+// faster up to 384 tokens (31.4 vs 33.4 us), the two kernels from 512 tokens
+// (35.5 vs 39.6 us; 4.30 vs 7.80 ms at 128K tokens).  GDN_ALGO_AUTO and
+// GDN_ALGO_CHUNKED use the two kernels when the sequences average at least
+// this many tokens and the caller's workspace is large enough.
+constexpr int64_t kSplitMinAvgTokens = 512;
+
+bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
+  return num_seqs > 0 && total_tokens >= kSplitMinAvgTokens * num_seqs;
+}
 
 int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return INT32_MAX;
@@ -86,9 +97,10 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
                                   int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                                   gdn_algo algo) {
   if (num_seqs < 0 || total_tokens < 0 || check_heads(h_k, h_v, d_k, d_v) != GDN_OK) return 0;
-  if (algo == GDN_ALGO_SCAN) return 0;
+  if (algo == GDN_ALGO_SCAN || algo == GDN_ALGO_CHUNKED_FUSED) return 0;
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return 0;
-  return gdn::chunked_workspace_bytes(num_seqs, total_tokens, h_k, h_v, d_k, d_v);
+  if (algo != GDN_ALGO_CHUNKED_SPLIT && !split_preferred(num_seqs, total_tokens)) return 0;
+  return gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
 }
 
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
@@ -98,7 +110,8 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
                        float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
                        gdn_stream_t stream) {
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
-  if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED)
+  if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED &&
+      algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
   gdn_status st = check_heads(h_k, h_v, d_k, d_v);
@@ -118,7 +131,9 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     if (a < b + state_bytes && b < a + state_bytes) return GDN_ERR_INVALID_ARG;
   }
   const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
-  if (algo == GDN_ALGO_CHUNKED && !chunk_ok)
+  const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
+                          algo == GDN_ALGO_CHUNKED_SPLIT;
+  if (chunk_only && !chunk_ok)
     return dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE;
 
   gdn::PrefillArgs a{};
@@ -135,7 +150,7 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
   bool run_scan = true, run_chunk = false;
   if (algo == GDN_ALGO_SCAN) {
     a.min_chunk_len = INT32_MAX;
-  } else if (algo == GDN_ALGO_CHUNKED) {
+  } else if (chunk_only) {
     a.min_chunk_len = 0;
     run_scan = false;
     run_chunk = true;
@@ -144,17 +159,28 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     run_chunk = chunk_ok && total_tokens >= a.min_chunk_len;
     run_scan = !(num_seqs == 1 && run_chunk);
   }
-  if (run_chunk) {
-    const size_t need = gdn::chunked_workspace_bytes(num_seqs, total_tokens, h_k, h_v, d_k, d_v);
-    if (workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
-    if (need > 0 && !workspace) return GDN_ERR_NULL_POINTER;
+  // The chunked evaluation runs as one fused kernel, or as two kernels meeting
+  // in the caller's workspace (forced by GDN_ALGO_CHUNKED_SPLIT; otherwise when
+  // the sequences are long enough and the workspace is large enough).
+  bool split = false;
+  if (run_chunk && algo != GDN_ALGO_CHUNKED_FUSED) {
+    const size_t need = gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
+    if (algo == GDN_ALGO_CHUNKED_SPLIT) {
+      if (!workspace) return GDN_ERR_NULL_POINTER;
+      if (workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    }
     if (workspace && !aligned16(workspace)) return GDN_ERR_MISALIGNED;
+    split = workspace && workspace_bytes >= need &&
+            (algo == GDN_ALGO_CHUNKED_SPLIT || split_preferred(num_seqs, total_tokens));
   }
   st = error_word(&a.err);
   if (st != GDN_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (run_chunk && gdn::launch_chunked(a, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (run_chunk) {
+    const cudaError_t e = split ? gdn::launch_chunked_split(a, workspace, s) : gdn::launch_chunked(a, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+  }
   if (run_scan && gdn::launch_scan(a, s) != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
 }

@@ -71,9 +71,12 @@ typedef enum {
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype; /* dtype of q, k, v and o */
 
 typedef enum {
-  GDN_ALGO_AUTO = 0,    /* per sequence: scan below the measured crossover length, else chunked */
-  GDN_ALGO_SCAN = 1,    /* token scan, state rows resident in registers (fp32 and bf16) */
-  GDN_ALGO_CHUNKED = 2  /* chunks of 64 tokens on tcgen05 tensor cores (bf16) */
+  GDN_ALGO_AUTO = 0,          /* per sequence: scan below the measured crossover length, else chunked */
+  GDN_ALGO_SCAN = 1,          /* token scan, state rows resident in registers (fp32 and bf16) */
+  GDN_ALGO_CHUNKED = 2,       /* chunks of 64 tokens on tcgen05 tensor cores (bf16); the library
+                                 picks the fused or the two-kernel form (see gdn_prefill) */
+  GDN_ALGO_CHUNKED_FUSED = 3, /* chunked, one fused kernel, no workspace */
+  GDN_ALGO_CHUNKED_SPLIT = 4  /* chunked, two kernels through the workspace (required) */
 } gdn_algo;
 
 /*
@@ -90,9 +93,17 @@ typedef enum {
  * cu_seqlens int32 device pointer of num_seqs+1 entries with cu[0] = 0,
  * non-decreasing, cu[num_seqs] = total_tokens; scale multiplies q (1 for the
  * plain reading o_t = S_t q_t).  algo selects the evaluation (see gdn_algo);
- * GDN_ALGO_CHUNKED with GDN_F32 returns GDN_ERR_UNSUPPORTED_DTYPE.
- * workspace must hold gdn_prefill_workspace_size(...) bytes (may be NULL when
- * that size is 0) and is not used after the launches complete.
+ * the chunked algorithms with GDN_F32 return GDN_ERR_UNSUPPORTED_DTYPE.
+ * workspace: scratch, 16-byte aligned, or NULL.  The chunked evaluation runs
+ * either as one fused kernel that needs no workspace, or as two kernels (the
+ * per-chunk state-independent work spread over all SMs, then the sequential
+ * state pass) that meet in the workspace.  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED
+ * take the two kernels when the sequences average at least 512 tokens (where
+ * they measured faster on GB300) and workspace_bytes is at least
+ * gdn_prefill_workspace_size(...), else the fused kernel;
+ * GDN_ALGO_CHUNKED_SPLIT always takes them and returns GDN_ERR_NULL_POINTER or
+ * GDN_ERR_WORKSPACE_TOO_SMALL without one.  Results agree within rounding; the
+ * workspace is not used after the launches complete.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
                        const float* beta, const float* state_in, float* state_out, void* o,
@@ -101,7 +112,10 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
                        float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
                        gdn_stream_t stream);
 
-/* Bytes of workspace gdn_prefill needs for these arguments (0 when none). */
+/* Bytes of workspace for the fastest gdn_prefill path with these arguments
+ * (0 when that path uses none); for GDN_ALGO_CHUNKED_SPLIT, the bytes it
+ * needs.  An upper bound computed from the host arguments: the 1 KB-rounded
+ * (N+1) int32 header + (T/64 + N + 1) * h_v * 33 KB. */
 size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
                                   int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                                   gdn_algo algo);

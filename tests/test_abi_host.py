@@ -65,6 +65,12 @@ def test_prefill_host_errors(lib):
     assert prefill(lib, state_in=FAKE + 16, state_out=FAKE) == 2   # partial overlap
     assert prefill(lib, n=0) == 0                        # nothing to do: OK, no launch
     assert prefill(lib, n=0, q=None) == 0
+    chunk = dict(d_k=128, d_v=32)                        # a shape the chunked kernels cover
+    assert prefill(lib, algo=4, **chunk) == 1            # two-kernel form without workspace
+    assert prefill(lib, algo=4, ws=FAKE, ws_bytes=16, **chunk) == 7
+    assert prefill(lib, algo=4, ws=FAKE + 8, ws_bytes=1 << 30, **chunk) == 5
+    assert prefill(lib, algo=3, dtype=0, **chunk) == 4   # chunked forms are bf16 only
+    assert prefill(lib, algo=3, d_k=64) == 3             # ... with d_k = 128
 
 
 def decode(lib, **kw):
@@ -88,6 +94,14 @@ def test_decode_host_errors(lib):
 
 def test_workspace_and_crossover_queries(lib):
     assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 1) == 0  # scan needs none
+    ws = lambda n, t, algo: lib.gdn_prefill_workspace_size(n, t, 16, 32, 128, 128, 1, algo)
+    assert ws(1, 4096, 3) == 0                           # fused chunked kernel: none
+    assert ws(1, 4096, 2) == ws(1, 4096, 4) > 0          # long sequences: two kernels
+    assert ws(4, 1000, 2) == 0 and ws(4, 1000, 0) == 0   # averaging 250 tokens: fused
+    assert ws(4, 1000, 4) > 0                            # unless the two kernels are forced
+    assert ws(4, 2048, 2) == ws(4, 2048, 4) > 0
+    # header (1 KB-rounded) + (T/64 + N + 1) per-chunk packages of 33 KB per value head
+    assert ws(4, 2048, 4) == 1024 + (2048 // 64 + 5) * 32 * 33792
     x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
     assert x > 0
     assert lib.gdn_prefill_crossover_tokens(16, 32, 128, 48, 1) == 2**31 - 1
