@@ -12,8 +12,11 @@ import torch
 from . import _lib
 from ._lib import GdnError, STATUS_NAMES
 
-__all__ = ["gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_size", "gdn_stream_status",
-           "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError", "STATUS_NAMES"]
+__all__ = ["gdn_prefill", "gdn_prefill_noalloc", "gdn_decode_step", "gdn_prefill_workspace_size",
+           "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
+           "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
+
+NOALLOC_SCRATCH_BYTES = 72 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 _DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
 
@@ -91,6 +94,32 @@ def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=N
                          dt, float(scale), _lib.ALGOS[algo], _ptr(workspace), ws_bytes,
                          _stream(stream))
     _lib.check(st, "gdn_prefill")
+    return o, state_out
+
+
+def gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, state_out, o, state_in=None, scale=1.0,
+                        stream=None):
+    """The two-kernel chunked prefill with the library's fixed scratch array
+    (gdn_prefill_noalloc in include/gdn.h), for callers that cannot allocate
+    device memory at call time.  Neither this wrapper nor the C entry point
+    allocates: the caller passes every output (o [T, h_v, d_v] bf16,
+    state_out [N, h_v, d_v, d_k] fp32).  Calls that overlap on the GPU race on
+    the shared scratch; order them (e.g. on one stream)."""
+    lib = _lib.load()
+    T, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    _require(k.shape == q.shape and v.shape[0] == T, "q/k/v shapes disagree")
+    _require(g.shape == (T, h_v) and beta.shape == (T, h_v), "g/beta must be [T, h_v]")
+    _require(o.shape == (T, h_v, d_v) and state_out.shape == (N, h_v, d_v, d_k),
+             "o / state_out shapes")
+    for t in (q, k, v, g, beta, cu_seqlens, o, state_out):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    st = lib.gdn_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                                 _ptr(state_out), _ptr(o), _ptr(cu_seqlens), N, T, h_k, h_v, d_k,
+                                 d_v, dt, float(scale), _stream(stream))
+    _lib.check(st, "gdn_prefill_noalloc")
     return o, state_out
 
 

@@ -34,7 +34,8 @@
  *
  * Ownership.  The caller owns every buffer; the library allocates no device
  * memory in any call below.  Scratch space for gdn_prefill is the caller's
- * `workspace` (size from gdn_prefill_workspace_size).
+ * `workspace` (size from gdn_prefill_workspace_size); gdn_prefill_noalloc
+ * uses a fixed array the library holds instead.
  *
  * Asynchrony.  Calls are ordered on the caller's `stream` and return after
  * the launches are enqueued.  Errors that the host can see (NULL pointers,
@@ -119,6 +120,42 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
 size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
                                   int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                                   gdn_algo algo);
+
+/*
+ * gdn_prefill_noalloc — gdn_prefill with GDN_ALGO_CHUNKED_SPLIT (the
+ * two-kernel chunked evaluation), taking its scratch from a fixed array of
+ * GDN_NOALLOC_SCRATCH_BYTES that the library holds in device memory instead of
+ * a caller workspace.  The source pages have no counterpart: it exists for
+ * callers that cannot allocate device memory when they call in, such as a host
+ * framework whose memory pool owns the device and hands its plugins no
+ * scratch buffer, or a serving loop that must not call cudaMalloc / cudaFree
+ * (they can synchronise the device and stall every stream in flight).  It
+ * allocates nothing and calls no allocating routine.
+ *
+ * Arguments, layouts, ownership of the caller's buffers and asynchronous
+ * errors are those of gdn_prefill; dtype must be GDN_BF16, d_k 128 and d_v a
+ * multiple of 32 (else GDN_ERR_UNSUPPORTED_*).  Limit: returns
+ * GDN_ERR_WORKSPACE_TOO_SMALL, touching no device, when
+ * gdn_prefill_workspace_size(..., GDN_ALGO_CHUNKED_SPLIT) for these arguments
+ * exceeds GDN_NOALLOC_SCRATCH_BYTES (72 MiB: e.g. one 4,096-token sequence at
+ * 32 value heads needs 71.4 MB); larger problems go through gdn_prefill with a
+ * workspace.
+ *
+ * Set-up: the first call with a given device current looks up that device's
+ * copy of the array (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Sharing: every call on a device uses the same array.
+ * Nothing in it has to start at zero (each call writes what it later reads),
+ * but calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on it: order them, e.g. on one stream.  The array takes
+ * GDN_NOALLOC_SCRATCH_BYTES of each device where the library's code is loaded.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)72 << 20)
+
+gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, const float* state_in, float* state_out,
+                               void* o, const int32_t* cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t h_k, int32_t h_v, int32_t d_k,
+                               int32_t d_v, gdn_dtype dtype, float scale, gdn_stream_t stream);
 
 /*
  * gdn_decode_step — one token for each of `batch` independent sequences,

@@ -73,6 +73,21 @@ def test_prefill_host_errors(lib):
     assert prefill(lib, algo=3, d_k=64) == 3             # ... with d_k = 128
 
 
+def test_noalloc_host_errors(lib):
+    """The allocation-free prefill refuses, without touching a device, problems
+    whose scratch exceeds its fixed array and arguments gdn_prefill refuses."""
+    def call(n=1, t=64, h_k=1, h_v=2, d_k=128, d_v=32, dtype=1):
+        return lib.gdn_prefill_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, n, t,
+                                       h_k, h_v, d_k, d_v, dtype, 1.0, None)
+    big = 1 << 20   # 1M tokens at 2 value heads: ~1.1 GB of scratch
+    assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 72 << 20
+    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 72 << 20
+    assert call(t=big) == 7                              # GDN_ERR_WORKSPACE_TOO_SMALL
+    assert call(d_k=64) == 3                             # chunked needs d_k = 128
+    assert call(dtype=0) == 4                            # and bf16
+    assert call(n=-1) == 2
+
+
 def decode(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE, b=1, h_k=1, h_v=1,
              d_k=16, d_v=16, dtype=1, scale=1.0, stream=None)
