@@ -219,13 +219,23 @@ def cpu_baseline(d, w, budget_s=12.0):
 
 
 # ---------------------------------------------------------------- our arm
+def max_over_ranks(x, device):
+    """Largest value of x over all ranks (timing: the slowest rank sets the step)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--algo", default="auto", choices=["auto", "scan", "chunked"])
+    ap.add_argument("--algo", default="auto",
+                    choices=["auto", "scan", "chunked", "chunked_fused", "chunked_split"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--sweep", action="store_true",
@@ -251,6 +261,7 @@ def main():
                                                         gdn_prefill_crossover_tokens,
                                                         gdn_prefill_workspace_size,
                                                         gdn_stream_status, inputs)
+    from gated_deltanet_linear_recurrence_gb300.shard import seq_shard
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -264,8 +275,13 @@ def main():
 
     w = inputs.WORKLOADS[WORKLOAD]
     h_k, h_v, d_k, d_v = w["h_k"], w["h_v"], w["d_k"], w["d_v"]
-    T = sum(w["lengths"])
-    d = inputs.make_prefill(w["lengths"], h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + rank)
+    # weak scaling: a global batch of one prompt per rank, split by sequences
+    # (no exchange between ranks); rank r draws its own prompt's inputs
+    lengths_all = list(w["lengths"]) * world
+    n0, n1 = seq_shard(inputs.cu_from_lengths(lengths_all), rank, world)
+    lengths = lengths_all[n0:n1]
+    T = sum(lengths)
+    d = inputs.make_prefill(lengths, h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + n0)
     x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     o = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
     st = torch.empty((1, h_v, d_v, d_k), dtype=torch.float32, device=dev)
@@ -309,16 +325,14 @@ def main():
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1e3)
     # chunked with workspace: plan + prepare + chain kernels; fused or scan: one kernel
-    launches_per_step = 3 if (algo_used == "chunked" and ws_n > 0) else 1
+    launches_per_step = 3 if (algo_used.startswith("chunked") and ws_n > 0) else 1
 
     # roofline of the prefill kernel (one launch per step)
-    if algo_used == "chunked":
+    if algo_used.startswith("chunked"):
         flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
         split = ws_n > 0
@@ -392,7 +406,8 @@ def main():
         "config": {"workload": f"{WORKLOAD} (B=1, T=4096, H_k=16, H_v=32, d_k=d_v=128, bf16 "
                                "q/k/v, fp32 g/beta/state, zero initial state)",
                    "global_batch": world, "seq_len": T,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "parallelism": (f"{world} ranks, one prompt each (sequence shards, no "
+                                   "exchange)") if world > 1 else "single GPU",
                    "algo": algo_used, "l2": "flushed between timed steps (2x L2 buffer written)"},
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,

@@ -63,6 +63,7 @@
 #include <mutex>
 
 #include "params.h"
+#include "per_device.h"
 #include "rows.cuh"
 #include "tc.cuh"
 #include "chunk_common.cuh"
@@ -595,11 +596,10 @@ cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream) {
       !encode_2d(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, kDVS, kC, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_prefill_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static PerDeviceOnce attrs;
+  const cudaError_t attr_err = attrs.run([] {
+    return cudaFuncSetAttribute(chunk_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   ChunkParams p;

@@ -40,6 +40,7 @@
 
 #include "chunk_common.cuh"
 #include "params.h"
+#include "per_device.h"
 #include "rows.cuh"
 #include "tc.cuh"
 
@@ -685,14 +686,14 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
       !encode_map(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, kDVS, kC, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_prepare_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(chunk_chain_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
+  static PerDeviceOnce attrs;
+  const cudaError_t attr_err = attrs.run([] {
+    cudaError_t e = cudaFuncSetAttribute(chunk_prepare_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kChainSmem);
+    return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
   SplitParams p;
