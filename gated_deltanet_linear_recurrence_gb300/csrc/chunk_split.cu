@@ -20,10 +20,12 @@
 // 3-stage ring next to the TMA'd Q, K and V slice:
 //   U~ = (T b) V_s,  D = [-W; Q] S^T,  U = U~ + D_top,
 //   S^T <- Gamma_n S^T + K^T (decay U),  O = Gamma D_bottom + P U.
-// Only D, U and the state update are on the chunk-to-chunk critical path: U~
-// of chunk c+1 is issued as soon as its stage has landed (it runs while chunk
-// c's U is formed), P U of chunk c runs while chunk c's state is staged for the
-// next chunk, and chunk c's output is written while chunk c+1's D product runs.
+// Warp roles: a producer warp (copies), an MMA warp (one thread issues every
+// product; an issue blocks while the tensor pipe is busy, so it gets a warp of
+// its own) and four epilogue warps, handing over through mbarriers.  Only D,
+// U, the state update and the state's staging are on the chunk-to-chunk
+// critical path: U~ of chunk c+1 and P U of chunk c run while chunk c's state
+// is staged, and chunk c's output is written while chunk c+1's U is formed.
 // chunk_plan_kernel computes each sequence's first package index (an exclusive
 // prefix sum of its chunk count) into the workspace header and records an
 // inconsistent cu_seqlens in the error word.
@@ -339,10 +341,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 }
 
 // ------------------------------------------------------------------ chain
-constexpr int kChainThreads = 128;
-constexpr int kChainKernelThreads = kChainThreads + 32;  // + producer warp
-constexpr int kProducerWarp = 4;
-constexpr uint32_t kBarChain = 1, kBarU = 2, kBarO = 3;  // all 4 warps; warps 0-1; warps 2-3
+constexpr int kChainThreads = 128;                       // epilogue warps 0-3
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kChainKernelThreads = kChainThreads + 64;  // + producer and MMA warps
 constexpr int kStages = 3;
 // Main stage: per d_k half kb [-W | Q | K] (8 KB each; [-W; Q] is one 128-row
 // operand), then T b (8 KB) and the V slice (4 KB); released once the chunk's
@@ -403,13 +404,19 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
   const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
   const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CC_MISC);  // main stages
+  // mbarriers.  full/tfull: TMA and bulk copies landed; empty: the stage's MMAs
+  // are done (tcgen05.commit); tempty: warps 2-3 wrote the chunk's output.
+  // bar_d, bar_s, bar_o: D, the state update, P U complete (tcgen05.commit);
+  // bar_u: warps 0-1 staged U; bar_ss: warps 0-3 staged the state.
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CC_MISC);
   uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;                              // tail stages
+  uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + kStages;
-  uint64_t* bar_d = tempty + kStages;  // [-W; Q] S^T (and every earlier MMA)
-  uint64_t* bar_s = bar_d + 1;         // state update
-  uint64_t* bar_o = bar_s + 1;         // P U, one barrier per chunk parity
+  uint64_t* bar_d = tempty + kStages;
+  uint64_t* bar_s = bar_d + 1;
+  uint64_t* bar_u = bar_s + 1;
+  uint64_t* bar_ss = bar_u + 1;
+  uint64_t* bar_o = bar_ss + 1;  // one per chunk parity
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, kChainTmemCols);
@@ -420,10 +427,12 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], 1);
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 1);
+      tc::mbar_init(&tempty[i], 64);
     }
     tc::mbar_init(bar_d, 1);
     tc::mbar_init(bar_s, 1);
+    tc::mbar_init(bar_u, 64);
+    tc::mbar_init(bar_ss, kChainThreads);
     tc::mbar_init(&bar_o[0], 1);
     tc::mbar_init(&bar_o[1], 1);
     tc::fence_mbar_init();
@@ -441,13 +450,11 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
       tc::prefetch_tmap(&tm_v);
-      for (int c = 0; c < nchunks; ++c) {
+      for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c % kStages;
         const uint8_t* pkg = p.packages + (first_item + (int64_t)c * p.h_v) * kPkgBytes;
-        if (c >= kStages && !tc::mbar_wait(&empty[st], ((c / kStages) - 1) & 1)) {
-          raise_error(p.err, kErrDeviceTimeout);
-          break;
-        }
+        if (c >= kStages) ok = tc::mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+        if (!ok) break;
         uint8_t* dst = smem + st * kMain;
         const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
         uint64_t* fb = &full[st];
@@ -460,41 +467,81 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
         }
         bulk_g2s(dst + SC_TA, pkg + kPkgTA, 8192, fb);
         tc::tma_load_2d(dst + SC_V, &tm_v, h * p.d_v + s * kDVS, y, fb);
-        if (c >= kStages && !tc::mbar_wait(&tempty[st], ((c / kStages) - 1) & 1)) {
-          raise_error(p.err, kErrDeviceTimeout);
-          break;
-        }
+        if (c >= kStages) ok = tc::mbar_wait(&tempty[st], ((c / kStages) - 1) & 1);
+        if (!ok) break;
         uint8_t* tl = smem + CC_TAIL + st * kTail;
         tc::mbar_arrive_expect_tx(&tfull[st], kTailTx);
         bulk_g2s(tl + TL_P, pkg + kPkgP, 8192, &tfull[st]);
         bulk_g2s(tl + TL_G, pkg + kPkgGates, 1024, &tfull[st]);
       }
     }
-  } else {
-    // Chain warps.  Warps 0-1 (TMEM lanes 0-63) form U; warps 2-3 (lanes 64-127)
-    // write the previous chunk's output meanwhile; all four stage the state.
-    const bool leader = tid == 0;
-    uint32_t ph_d = 0, ph_s = 0;
-    const uint32_t ss = sbase + CC_SS;
-    const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
-    int u_issued = -1;                       // last chunk whose U~ product is issued (leader)
-    auto issue_u = [&](int cu_) {  // U~ = (T b) V_s of chunk cu_ into TC_U0 + 32 (cu_ & 1)
-      const uint32_t stg = sbase + (cu_ % kStages) * kMain;
+  } else if (warp == kMmaWarp) {
+    // One thread issues every tensor-core product, in the order the chain needs
+    // them; issuing blocks while the tensor pipe is busy, so no epilogue work
+    // waits behind it.  (Measured on GB300: issuing from lane 0 of this warp is
+    // faster here than issuing from a converged warp under elect.sync.)  Per
+    // chunk c:  U~(c) -> [state staged] D(c) -> [U staged] S update(c) -> P U(c)
+    if (lane == 0) {
+      const uint32_t ss = sbase + CC_SS;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c % kStages;
+        const uint32_t stg = sbase + st * kMain;
+        const uint32_t tl = sbase + CC_TAIL + st * kTail;
+        ok = tc::mbar_wait(&full[st], (c / kStages) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc::mma_bf16(tmem + TC_U0 + 32 * (cu_ & 1),
-                     tc::smem_desc(stg + SC_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
-                     tc::smem_desc(stg + SC_V + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_UT,
-                     kk > 0);
-      u_issued = cu_;
-    };
+        for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V_s
+          tc::mma_bf16(tmem + TC_U0 + 32 * (c & 1),
+                       tc::smem_desc(stg + SC_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(stg + SC_V + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_UT,
+                       kk > 0);
+        ok = tc::mbar_wait(bar_ss, c & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // D = [-W; Q] S_s^T
+          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + TC_D0 + 32 * (c & 1),
+                       tc::smem_desc(stg + ko + SC_W, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_WQ, kk > 0);
+        }
+        tc::mma_commit(bar_d);
+        ok = tc::mbar_wait(bar_u, c & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
+          tc::mma_bf16(tmem + TC_S,
+                       tc::smem_desc(stg + SC_K + kk * 2048, kHalf, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(sbase + CC_UK + kk * 1024, 4096, 512, tc::kLayoutSw64),
+                       IDC_SU, 1);
+        tc::mma_commit(bar_s);
+        tc::mma_commit(&empty[st]);  // -W, Q, K, T b, V of the stage consumed
+        ok = tc::mbar_wait(&tfull[st], (c / kStages) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
+          tc::mma_bf16(tmem + TC_O0 + 32 * (c & 1),
+                       tc::smem_desc(tl + TL_P - 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
+                       tc::smem_desc(sbase + CC_UB + kk * 1024, 4096, 512, tc::kLayoutSw64),
+                       IDC_PU, kk > 0);
+        tc::mma_commit(&bar_o[c & 1]);
+      }
+    }
+  } else {
+    // Epilogue warps.  Warps 0-1 (TMEM lanes 0-63) form U; warps 2-3 (lanes
+    // 64-127) write the previous chunk's output meanwhile; all four stage the
+    // state.  Every hand-off is an mbarrier with a bounded wait.
+    const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
     // Output of chunk cp (warps 2-3): O = Gamma Q S^T + P U for rows r = lanes
     // 64-127, then release its tail stage.
     auto finish_output = [&](int cp) {
       const int stp = cp % kStages;
       const float* gp = reinterpret_cast<const float*>(smem + CC_TAIL + stp * kTail + TL_G);
-      // chunk cp + 2 commits to the same barrier only after this wait (the
-      // chain barrier of chunk cp + 1 orders them), so the parity is unambiguous
+      // P U of chunk cp + 2 is issued only after this chunk's output is done
+      // (warps 2-3 then stage chunk cp + 1's state), so the parity is unambiguous
       ok = tc::mbar_wait(&bar_o[cp & 1], (cp >> 1) & 1) && ok;
       tc::fence_after_sync();
       const int64_t t0p = t_beg + (int64_t)cp * kC;
@@ -519,11 +566,11 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
         }
       }
       tc::fence_before_sync();
-      tc::named_sync(kBarO, 64);
-      if (tid == 64) tc::mbar_arrive(&tempty[stp]);
+      tc::mbar_arrive(&tempty[stp]);
     };
-    // S (fp32, thread j holds column j of the slice) -> bf16 operand copy, then
-    // Gamma_n of chunk cn applied in TMEM (the update MMA accumulates onto it).
+    // S (fp32, thread j holds column j of the slice) -> bf16 operand copy for
+    // chunk cn's D, then Gamma_n of chunk cn applied in TMEM (the update MMA
+    // accumulates onto it); then tell the MMA warp.
     auto stage_state = [&](float (&sc)[32], int cn) {
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_SS, tid * 64 + c4 * 16, sc + 8 * c4);
@@ -533,6 +580,9 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
       tc::tmem_st32(tmem + lane_base + TC_S, sc);
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_ss);
     };
     {  // initial state
       float sc[32];
@@ -545,30 +595,12 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       } else {
         stage_state(sc, 0);
       }
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      ok = tc::named_sync_and(kBarChain, kChainThreads, ok);
-      tc::fence_after_sync();
     }
     for (int c = 0; c < nchunks && ok; ++c) {
       const int st = c % kStages;
-      const uint32_t stg = sbase + st * kMain;
       const float* gates = reinterpret_cast<const float*>(smem + CC_TAIL + st * kTail + TL_G);
-      if (leader) {
-        ok = tc::mbar_wait(&full[st], (c / kStages) & 1) && ok;
-        tc::fence_after_sync();
-        if (u_issued < c) issue_u(c);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // D = [-W; Q] S_s^T
-          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + TC_D0 + 32 * (c & 1),
-                       tc::smem_desc(stg + ko + SC_W, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_WQ, kk > 0);
-        }
-        tc::mma_commit(bar_d);
-      }
       if (warp < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
-        ok = tc::mbar_wait(bar_d, ph_d & 1) && ok;
+        ok = tc::mbar_wait(bar_d, c & 1) && ok;
         tc::fence_after_sync();
         const float dec_r = gates[64 + rl];
         float u[32], d[32];
@@ -584,57 +616,24 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
         for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_UK, rl * 64 + c4 * 16, u + 8 * c4);
         tc::fence_proxy_async();
         tc::fence_before_sync();
-        tc::named_sync(kBarU, 64);
-        tc::fence_after_sync();
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U): the next chunk waits on this
-            tc::mma_bf16(tmem + TC_S,
-                         tc::smem_desc(stg + SC_K + kk * 2048, kHalf, 1024, tc::kLayoutSw128),
-                         tc::smem_desc(sbase + CC_UK + kk * 1024, 4096, 512, tc::kLayoutSw64),
-                         IDC_SU, 1);
-          tc::mma_commit(bar_s);
-          const uint32_t tl = sbase + CC_TAIL + st * kTail;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127) while the state is staged
-            tc::mma_bf16(tmem + TC_O0 + 32 * (c & 1),
-                         tc::smem_desc(tl + TL_P - 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
-                         tc::smem_desc(sbase + CC_UB + kk * 1024, 4096, 512, tc::kLayoutSw64),
-                         IDC_PU, kk > 0);
-          tc::mma_commit(&bar_o[c & 1]);
-          // the next chunk's U~, if its stage has landed
-          if (c + 1 < nchunks &&
-              tc::mbar_try_wait(&full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
-            tc::fence_after_sync();
-            issue_u(c + 1);
-          }
-        }
+        tc::mbar_arrive(bar_u);
       } else if (c > 0) {
         finish_output(c - 1);  // warps 2-3, while U is formed
       }
-      ++ph_d;
-      ok = tc::mbar_wait(bar_s, ph_s & 1) && ok;
+      ok = tc::mbar_wait(bar_s, c & 1) && ok;
       tc::fence_after_sync();
-      ++ph_s;
-      if (leader) tc::mbar_arrive(&empty[st]);  // -W, Q, K, T b and V of the stage consumed
-      {
-        float sc[32];
-        tc::tmem_ld32(tmem + lane_base + TC_S, sc);
-        if (c == nchunks - 1) {
+      float sc[32];
+      tc::tmem_ld32(tmem + lane_base + TC_S, sc);
+      if (c == nchunks - 1) {
 #pragma unroll
-          for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
-        } else {
-          stage_state(sc, c + 1);
-        }
+        for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+      } else {
+        stage_state(sc, c + 1);
       }
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      ok = tc::named_sync_and(kBarChain, kChainThreads, ok);
-      tc::fence_after_sync();
     }
     if (ok && nchunks > 0 && warp >= 2) finish_output(nchunks - 1);  // the last chunk's output
   }
-  if (!ok && tid == 0) raise_error(p.err, kErrDeviceTimeout);
+  if (!ok) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
