@@ -16,7 +16,7 @@ __all__ = ["gdn_prefill", "gdn_prefill_noalloc", "gdn_decode_step", "gdn_prefill
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
-NOALLOC_SCRATCH_BYTES = 72 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
+NOALLOC_SCRATCH_BYTES = 96 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 _DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
 

@@ -5,27 +5,29 @@
 // Apple Silicon", section "Qwen creates three distinct workload shapes") splits
 // into work that does not depend on the state — per chunk of 64 tokens and
 // value head: gates, the Q K^T / K K^T masks, the triangular solve
-// T = (I + A)^{-1}, W = T diag(b Gamma) K — and the sequential state pass.
+// T = (I + A)^{-1}, W = T diag(b Gamma) K, U~ = T diag(b) V — and the
+// sequential state pass.
 // chunk_prepare_kernel does the first part once per (chunk, value head), spread
 // over every SM, and writes a "package" per item to the workspace, already in
 // the swizzled shared-memory layout the tensor cores read:
 //
 //   [ -W half 0 | -W half 1 ]  bf16 [r][j], K-major SWIZZLE_128B, 2 x 8 KB
 //   [ P ]                      bf16 [r][i], 8 KB   (e^{gamma_r - gamma_i} q_r.k_i, i <= r)
-//   [ T b ]                    bf16 [r][i], 8 KB   (T diag(beta))
+//   [ U~ slices 0..3 ]         bf16 [r][32 values of d_v], 64-byte rows with the
+//                              SW64 XOR pattern, 4 x 4 KB  (U~ = T diag(beta) V)
 //   [ gates ]                  fp32 Gamma[64], decay[64] (e^{gamma_n - gamma_r}), Gamma_n
 //
 // chunk_chain_kernel walks each (sequence, value head, 32-row slice of d_v) in
 // chunk order with the fp32 state in TMEM, bulk-copying the packages into a
 // 3-stage ring next to the TMA'd Q, K and V slice:
-//   U~ = (T b) V_s,  D = [-W; Q] S^T,  U = U~ + D_top,
+//   D = [-W; Q] S^T,  U = U~ + D_top,
 //   S^T <- Gamma_n S^T + K^T (decay U),  O = Gamma D_bottom + P U.
 // Warp roles: a producer warp (copies), an MMA warp (one thread issues every
 // product; an issue blocks while the tensor pipe is busy, so it gets a warp of
 // its own) and four epilogue warps, handing over through mbarriers.  Only D,
 // U, the state update and the state's staging are on the chunk-to-chunk
-// critical path: U~ of chunk c+1 and P U of chunk c run while chunk c's state
-// is staged, and chunk c's output is written while chunk c+1's U is formed.
+// critical path: P U of chunk c runs while chunk c's state is staged, and
+// chunk c's output is written while chunk c+1's U is formed.
 // chunk_plan_kernel computes each sequence's first package index (an exclusive
 // prefix sum of its chunk count) into the workspace header and records an
 // inconsistent cu_seqlens in the error word.
@@ -49,8 +51,9 @@
 namespace gdn {
 
 // Workspace layout (shared with the host-side size computation).
-constexpr uint32_t kPkgW = 0, kPkgP = 16384, kPkgTA = 24576, kPkgGates = 32768;
-constexpr uint32_t kPkgBytes = 33792;  // 33 KB, a multiple of 1024 (swizzle phase)
+constexpr uint32_t kPkgW = 0, kPkgP = 16384, kPkgU = 24576, kPkgGates = 40960;
+constexpr uint32_t kPkgUSlice = 4096;  // U~ of one 32-wide slice of d_v
+constexpr uint32_t kPkgBytes = 41984;  // 41 KB, a multiple of 1024 (swizzle phase)
 
 size_t split_header_bytes(int32_t num_seqs) {
   return ((size_t)(num_seqs + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
@@ -89,8 +92,18 @@ __device__ __forceinline__ bool seq_range(const SplitParams& p, int n, int64_t& 
            (n == p.num_seqs - 1 && t1 != p.total_tokens));
 }
 
+// Programmatic dependent launch: the next kernel in the stream may start its
+// set-up now; and this kernel's reads of the previous kernel's results wait here.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(256) chunk_plan_kernel(const SplitParams p) {
+  allow_dependents();  // the prepare kernel's CTAs wait for this table themselves
   __shared__ int32_t warp_sums[8];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -128,23 +141,51 @@ __global__ void __launch_bounds__(256) chunk_plan_kernel(const SplitParams p) {
   if (threadIdx.x == 0) p.chunk_base[p.num_seqs] = carry;
 }
 
+// ------------------------------------------------------------------ bulk copies
+// global -> shared, completing on an mbarrier
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+// shared -> global (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(tc::smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+// Wait until every bulk copy this thread issued has read its shared-memory
+// source (the writes complete before the grid does).
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+
 // ------------------------------------------------------------------ prepare
 constexpr int kPrepThreads = 256;
 constexpr uint32_t kBarAll = 1, kBarGateP = 2;
 // shared memory of the prepare kernel
 constexpr uint32_t PP_KQ = 0;                      // per d_k half: [Q 8K][K 8K]
-constexpr uint32_t PP_TB = 32768;                  // T diag(b Gamma) bf16, SW128 (solve scratch first)
-constexpr uint32_t PP_MF = PP_TB + 8192;           // A, then T: fp32 [64][kLdM]
-constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;  // gamma, Gamma, beta, decay
-constexpr uint32_t PP_MISC = PP_GATE + 4 * 64 * 4;
+constexpr uint32_t PP_V = 32768;                   // V, two 64-column boxes [t][64], SW128
+constexpr uint32_t PP_TB = PP_V + 16384;           // T diag(b Gamma) bf16, SW128 (solve scratch first)
+constexpr uint32_t PP_TA = PP_TB + 8192;           // T diag(b) bf16, SW128
+constexpr uint32_t PP_MF = PP_TA + 8192;           // A, then T: fp32 [64][kLdM]
+// gates: Gamma[64], decay[64], Gamma_n (+pad) — the package's gates block as
+// laid out in the workspace — then gamma[64], beta[64]
+constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;
+constexpr uint32_t PP_MISC = PP_GATE + 5 * 64 * 4;
 constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
-constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W (0-127)
+constexpr uint32_t kPrepTmemCols = 256;  // G (cols 0-63), then W (0-127) and U~ (128-255)
 constexpr uint32_t IDP_G = tc::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDP_W = tc::idesc_bf16_f32(64, 128, false, true);
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
     chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -152,6 +193,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const int64_t item = blockIdx.x;
   const int64_t cid = item / p.h_v;
   const int h = (int)(item % p.h_v);
+  // The chain kernel may launch once every CTA of this grid has started; its
+  // CTAs need an SM without a prepare CTA, so they start as this grid drains.
+  allow_dependents();
+  wait_prerequisites();  // the chunk table of the plan kernel
   const int32_t total_chunks = p.chunk_base[p.num_seqs];
   if (cid >= total_chunks) return;
   // the sequence owning chunk cid: last n with chunk_base[n] <= cid (skipping empty ones)
@@ -169,11 +214,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
   float* MF = reinterpret_cast<float*>(smem + PP_MF);
   float* YF = reinterpret_cast<float*>(smem + PP_TB);
-  float* gam = reinterpret_cast<float*>(smem + PP_GATE);
-  float *Gam = gam + 64, *bet = gam + 128, *dec = gam + 192;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);
+  float* gsm = reinterpret_cast<float*>(smem + PP_GATE);
+  float *Gam = gsm, *dec = gsm + 64, *gam = gsm + 192, *bet = gsm + 256;
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);  // Q, K
   uint64_t* bar_mma = bar_tma + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 2);
+  uint64_t* bar_v = bar_tma + 2;                                     // V (needed only for U~)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 3);
   const uint32_t sbase = tc::smem_u32(smem);
 
   if (pw == 0) {
@@ -183,13 +229,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (pt == 0) {
     tc::mbar_init(bar_tma, 1);
     tc::mbar_init(bar_mma, 1);
+    tc::mbar_init(bar_v, 1);
     tc::fence_mbar_init();
     tc::mbar_arrive_expect_tx(bar_tma, 32768);
+    tc::mbar_arrive_expect_tx(bar_v, 16384);
     const int32_t y = static_cast<int32_t>(t0);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
       tc::tma_load_2d(smem + PP_KQ + kb * 16384, &tm_q, hk * kDK + 64 * kb, y, bar_tma);
       tc::tma_load_2d(smem + PP_KQ + kb * 16384 + 8192, &tm_k, hk * kDK + 64 * kb, y, bar_tma);
+      // columns past this head's d_v (d_v < 128) belong to the next head or
+      // lie outside the tensor (zero fill); the slices built from them are
+      // never written
+      tc::tma_load_2d(smem + PP_V + kb * 8192, &tm_v, h * p.d_v + 64 * kb, y, bar_v);
     }
   }
   float gr = 0.f, br = 0.f;
@@ -231,17 +283,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       bet[pt] = br;
       tc::named_sync(kBarGateP, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
-      float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
-      gout[pt] = Gam[pt];
-      gout[64 + pt] = dec[pt];
-      if (pt == 0) gout[128] = Gam[kC - 1];
+      if (pt == 0) gsm[128] = Gam[kC - 1];
     }
     ok = tc::mbar_wait(bar_mma, 0);
     tc::fence_after_sync();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
   }
   if (ok) {
-    // masks: P rows (subpartitions 0,1) to the package, A rows (2,3) to MF
+    // masks: P rows (subpartitions 0,1) over Q's first half (dead once G is
+    // done) in the package's layout, A rows (2,3) to MF
     const int half = pw >> 2, i0 = 32 * half;
     float a[32];
     tc::tmem_ld32(tmem + lane_base + 32 * half, a);
@@ -259,7 +309,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
       }
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(pkg + kPkgP, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+      for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(smem + PP_KQ, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
     } else {
       const int r = 32 * (sp - 2) + lane;
       const float g_r = gam[r], b_r = bet[r];
@@ -283,7 +333,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
     unit_lower_inverse<kBarAll, kPrepThreads>(MF, YF, pt, lane);
 
-    {  // T diag(b Gamma) to shared memory (W operand), T diag(b) to the package
+    {  // T diag(b Gamma) and T diag(b) to shared memory (W and U~ operands)
       const int r = pt >> 2, q = pt & 3;
 #pragma unroll
       for (int c8 = 0; c8 < 2; ++c8) {
@@ -298,7 +348,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
         float xb[8] = {xa[0] * G0.x, xa[1] * G0.y, xa[2] * G0.z, xa[3] * G0.w,
                        xa[4] * G1.x, xa[5] * G1.y, xa[6] * G1.z, xa[7] * G1.w};
-        st_chunk<3>(pkg + kPkgTA, r * 128 + (2 * q + c8) * 16, xa);
+        st_chunk<3>(smem + PP_TA, r * 128 + (2 * q + c8) * 16, xa);
         st_chunk<3>(smem + PP_TB, r * 128 + (2 * q + c8) * 16, xb);
       }
     }
@@ -306,18 +356,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc::fence_before_sync();
     tc::named_sync(kBarAll, kPrepThreads);
     tc::fence_after_sync();
-    if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (overwrites G's columns)
+    if (pt == 64 && tc::mbar_wait(bar_v, 0)) {  // (on a timeout nothing commits: all time out)
+      tc::fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
+      for (int kk = 0; kk < 4; ++kk)  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
         tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_TB + kk * 32, 16, 1024, tc::kLayoutSw128),
                      tc::smem_desc(sbase + PP_KQ + 8192 + kk * 2048, 16384, 1024, tc::kLayoutSw128),
                      IDP_W, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V: M=64 N=128 K=64
+        tc::mma_bf16(tmem + 128, tc::smem_desc(sbase + PP_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
+                     tc::smem_desc(sbase + PP_V + kk * 2048, 8192, 1024, tc::kLayoutSw128), IDP_W,
+                     kk > 0);
       tc::mma_commit(bar_mma);
     }
     ok = tc::mbar_wait(bar_mma, 1);
     tc::fence_after_sync();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (ok) {  // -W (M=64 accumulator: row 16 sp + lane on lanes 0-15) to the package
+    if (ok) {  // -W over K, U~ over V (M=64 accumulators: row 16 sp + lane on lanes 0-15)
       const int r = 16 * sp + lane;
       float w[32];
 #pragma unroll
@@ -328,16 +384,33 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           for (int e = 0; e < 32; ++e) w[e] = -w[e];
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8)
-            st_chunk<3>(pkg + kPkgW + half * 8192, r * 128 + (4 * q2 + c8) * 16, w + 8 * c8);
+            st_chunk<3>(smem + PP_KQ + half * 16384 + 8192, r * 128 + (4 * q2 + c8) * 16,
+                        w + 8 * c8);
+        }
+        tc::tmem_ld32(tmem + lane_base + 128 + 64 * half + 32 * q2, w);
+        const int sl = 2 * half + q2;  // 32-wide slice of d_v
+        if (lane < 16 && sl * kDVS < p.d_v) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_chunk<2>(smem + PP_V + sl * kPkgUSlice, r * 64 + c8 * 16, w + 8 * c8);
         }
       }
     }
+    tc::fence_proxy_async();  // staged package -> bulk copies
   }
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (pw == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
+  if (ok && pt == 0) {  // the package, in four coalesced bulk copies
+    bulk_s2g(pkg + kPkgW, smem + PP_KQ + 8192, 8192);
+    bulk_s2g(pkg + kPkgW + 8192, smem + PP_KQ + 16384 + 8192, 8192);
+    bulk_s2g(pkg + kPkgP, smem + PP_KQ, 8192);
+    bulk_s2g(pkg + kPkgU, smem + PP_V, (uint32_t)(p.d_v / kDVS) * kPkgUSlice);
+    bulk_s2g(pkg + kPkgGates, smem + PP_GATE, 1024);
+    bulk_commit_and_wait_read();  // the CTA's shared memory stays until it is read
+  }
 }
 
 // ------------------------------------------------------------------ chain
@@ -346,14 +419,14 @@ constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr int kChainKernelThreads = kChainThreads + 64;  // + producer and MMA warps
 constexpr int kStages = 3;
 // Main stage: per d_k half kb [-W | Q | K] (8 KB each; [-W; Q] is one 128-row
-// operand), then T b (8 KB) and the V slice (4 KB); released once the chunk's
-// state update is done.  Tail stage: P (8 KB) and the gates, released after the
-// chunk's output (one chunk later).  The 64 rows after T b and before each P
-// are valid shared memory, as M=128 operands whose other half is never read.
+// operand), then the slice's U~ (4 KB); released once the chunk's state update
+// is done.  Tail stage: P (8 KB) and the gates, released after the chunk's
+// output (one chunk later).  The 64 rows before each P are valid shared
+// memory, as an M=128 operand whose other half is never read.
 constexpr uint32_t kHalf = 24576;
-constexpr uint32_t SC_W = 0, SC_Q = 8192, SC_K = 16384, SC_TA = 2 * kHalf, SC_V = SC_TA + 8192;
-constexpr uint32_t kMain = SC_V + 4096;                                    // 61440
-constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + 8192 + 4096;
+constexpr uint32_t SC_W = 0, SC_Q = 8192, SC_K = 16384, SC_U = 2 * kHalf;
+constexpr uint32_t kMain = SC_U + kPkgUSlice;                              // 53248
+constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + kPkgUSlice;
 static_assert(kMainTx == kMain, "every main-stage byte arrives by TMA or bulk copy");
 constexpr uint32_t TL_P = 0, TL_G = 8192;
 constexpr uint32_t kTail = 9216;
@@ -366,27 +439,18 @@ constexpr uint32_t CC_MISC = CC_UK + 4096;
 constexpr uint32_t kChainSmem = CC_MISC + 256 + 1024;
 static_assert(kChainSmem <= 227 * 1024, "shared memory budget");
 static_assert(kMain % 1024 == 0 && kTail % 1024 == 0 && CC_TAIL % 1024 == 0 &&
-                  CC_SS % 1024 == 0 && SC_TA % 1024 == 0 && SC_V % 512 == 0,
+                  CC_SS % 1024 == 0 && SC_U % 512 == 0,
               "swizzled operands need 1024 / 512 byte alignment");
 constexpr uint32_t kChainTmemCols = 256;
-constexpr uint32_t TC_U0 = 0, TC_D0 = 64, TC_O0 = 128, TC_S = 192;  // U~, D, P U double-buffered
-constexpr uint32_t IDC_UT = tc::idesc_bf16_f32(128, 32, false, true);  // [T b; .] V_s
+constexpr uint32_t TC_D0 = 0, TC_O0 = 64, TC_S = 128;  // D and P U double-buffered
 constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, 32, false, true);  // [-W; Q] S^T
 constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, 32, true, true);   // K^T (decay U)
 constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, 32, false, true);  // [.; P] U (rows 64-127)
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-      : "memory");
-}
 
 __global__ void __launch_bounds__(kChainKernelThreads, 1)
     chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
+                       const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -401,7 +465,6 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
   const int64_t L = t_end - t_beg;
   if (L < p.min_len) return;  // the token scan owns this sequence
   const int nchunks = (int)((L + kC - 1) / kC);
-  const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
   const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;
 
   // mbarriers.  full/tfull: TMA and bulk copies landed; empty: the stage's MMAs
@@ -444,12 +507,13 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   bool ok = true;
+  wait_prerequisites();  // the packages and chunk table (set-up above overlapped the prepare)
+  const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
-      tc::prefetch_tmap(&tm_v);
       for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c % kStages;
         const uint8_t* pkg = p.packages + (first_item + (int64_t)c * p.h_v) * kPkgBytes;
@@ -465,8 +529,7 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
           tc::tma_load_2d(dst + kb * kHalf + SC_K, &tm_k, hk * kDK + 64 * kb, y, fb);
           bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
         }
-        bulk_g2s(dst + SC_TA, pkg + kPkgTA, 8192, fb);
-        tc::tma_load_2d(dst + SC_V, &tm_v, h * p.d_v + s * kDVS, y, fb);
+        bulk_g2s(dst + SC_U, pkg + kPkgU + s * kPkgUSlice, kPkgUSlice, fb);
         if (c >= kStages) ok = tc::mbar_wait(&tempty[st], ((c / kStages) - 1) & 1);
         if (!ok) break;
         uint8_t* tl = smem + CC_TAIL + st * kTail;
@@ -480,53 +543,45 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
     // them; issuing blocks while the tensor pipe is busy, so no epilogue work
     // waits behind it.  (Measured on GB300: issuing from lane 0 of this warp is
     // faster here than issuing from a converged warp under elect.sync.)  Per
-    // chunk c:  U~(c) -> [state staged] D(c) -> [U staged] S update(c) -> P U(c)
+    // chunk c:  [stage landed, state staged] D(c) -> [U staged] S update(c) -> P U(c)
     if (lane == 0) {
-      const uint32_t ss = sbase + CC_SS;
+      // Operand descriptors built once; a stage or K step only adds its byte
+      // offset / 16 to the start-address field (every address is below 256 KB).
+      const uint64_t dSS = tc::smem_desc(sbase + CC_SS, 4096, 512, tc::kLayoutSw64);
+      const uint64_t dUK = tc::smem_desc(sbase + CC_UK, 4096, 512, tc::kLayoutSw64);
+      const uint64_t dUB = tc::smem_desc(sbase + CC_UB, 4096, 512, tc::kLayoutSw64);
+      const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
+      const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
+      const uint64_t dP0 = tc::smem_desc(sbase + CC_TAIL + TL_P - 8192, 16, 1024, tc::kLayoutSw128);
       for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c % kStages;
-        const uint32_t stg = sbase + st * kMain;
-        const uint32_t tl = sbase + CC_TAIL + st * kTail;
+        const uint64_t so = (uint64_t)((st * kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
+        const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
+        const uint32_t td = tmem + TC_D0 + 32 * (c & 1), to2 = tmem + TC_O0 + 32 * (c & 1);
         ok = tc::mbar_wait(&full[st], (c / kStages) & 1);
         if (!ok) break;
-        tc::fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V_s
-          tc::mma_bf16(tmem + TC_U0 + 32 * (c & 1),
-                       tc::smem_desc(stg + SC_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(stg + SC_V + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_UT,
-                       kk > 0);
         ok = tc::mbar_wait(bar_ss, c & 1);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // D = [-W; Q] S_s^T
-          const uint32_t ko = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + TC_D0 + 32 * (c & 1),
-                       tc::smem_desc(stg + ko + SC_W, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(ss + kk * 1024, 4096, 512, tc::kLayoutSw64), IDC_WQ, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // D = [-W; Q] S_s^T
+          tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4), dSS + ((kk * 1024) >> 4),
+                       IDC_WQ, kk > 0);
         tc::mma_commit(bar_d);
         ok = tc::mbar_wait(bar_u, c & 1);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
-          tc::mma_bf16(tmem + TC_S,
-                       tc::smem_desc(stg + SC_K + kk * 2048, kHalf, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(sbase + CC_UK + kk * 1024, 4096, 512, tc::kLayoutSw64),
-                       IDC_SU, 1);
+          tc::mma_bf16(tmem + TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4), IDC_SU, 1);
         tc::mma_commit(bar_s);
-        tc::mma_commit(&empty[st]);  // -W, Q, K, T b, V of the stage consumed
+        tc::mma_commit(&empty[st]);  // -W, Q, K and U~ of the stage consumed
         ok = tc::mbar_wait(&tfull[st], (c / kStages) & 1);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
-          tc::mma_bf16(tmem + TC_O0 + 32 * (c & 1),
-                       tc::smem_desc(tl + TL_P - 8192 + kk * 32, 16, 1024, tc::kLayoutSw128),
-                       tc::smem_desc(sbase + CC_UB + kk * 1024, 4096, 512, tc::kLayoutSw64),
-                       IDC_PU, kk > 0);
+          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), IDC_PU, kk > 0);
         tc::mma_commit(&bar_o[c & 1]);
       }
     }
@@ -601,11 +656,23 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       const float* gates = reinterpret_cast<const float*>(smem + CC_TAIL + st * kTail + TL_G);
       if (warp < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
         ok = tc::mbar_wait(bar_d, c & 1) && ok;
+        // U~ arrived by bulk copy: observe the stage's own barrier before reading it
+        ok = tc::mbar_wait(&full[st], (c / kStages) & 1) && ok;
         tc::fence_after_sync();
         const float dec_r = gates[64 + rl];
         float u[32], d[32];
-        tc::tmem_ld32(tmem + lane_base + TC_U0 + 32 * (c & 1), u);
         tc::tmem_ld32(tmem + lane_base + TC_D0 + 32 * (c & 1), d);
+        const uint8_t* ut = smem + st * kMain + SC_U;  // this row of U~, bf16
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 q4 = *reinterpret_cast<const uint4*>(ut + tc::swizzle<2>(rl * 64 + j * 16));
+          const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            u[8 * j + 2 * e] = __uint_as_float(w4[e] << 16);
+            u[8 * j + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] += d[i];
 #pragma unroll
@@ -676,14 +743,14 @@ size_t split_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v
 
 cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv;  // mv: V in 64-column boxes for the prepare kernel's U~
   const uint64_t rows = a.total_tokens > 0 ? (uint64_t)a.total_tokens : 1;
   const void* qp = a.total_tokens > 0 ? a.q : a.state_out;
   const void* kp = a.total_tokens > 0 ? a.k : a.state_out;
   const void* vp = a.total_tokens > 0 ? a.v : a.state_out;
   if (!encode_map(&mq, qp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_map(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, kDVS, kC, CU_TENSOR_MAP_SWIZZLE_64B))
+      !encode_map(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static PerDeviceOnce attrs;
   const cudaError_t attr_err = attrs.run([] {
@@ -715,15 +782,29 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   p.err = a.err;
   chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
+  // prepare and chain launch with programmatic stream serialization: each may
+  // start its set-up before the kernel before it has finished (the kernels
+  // wait for that kernel's results with griddepcontrol.wait)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
   if (e != cudaSuccess) return e;
   if (p.max_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  chunk_prepare_kernel<<<(unsigned)p.max_items, kPrepThreads, kPrepSmem, stream>>>(mq, mk, p);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)p.max_items);
+  cfg.blockDim = dim3(kPrepThreads);
+  cfg.dynamicSmemBytes = kPrepSmem;
+  e = cudaLaunchKernelEx(&cfg, chunk_prepare_kernel, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)a.num_seqs * a.h_v * (a.d_v / kDVS);
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  chunk_chain_kernel<<<(unsigned)grid, kChainKernelThreads, kChainSmem, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kChainKernelThreads);
+  cfg.dynamicSmemBytes = kChainSmem;
+  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, mq, mk, p);
 }
 
 }  // namespace gdn

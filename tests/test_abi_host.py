@@ -80,8 +80,8 @@ def test_noalloc_host_errors(lib):
         return lib.gdn_prefill_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, n, t,
                                        h_k, h_v, d_k, d_v, dtype, 1.0, None)
     big = 1 << 20   # 1M tokens at 2 value heads: ~1.1 GB of scratch
-    assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 72 << 20
-    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 72 << 20
+    assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 96 << 20
+    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 96 << 20
     assert call(t=big) == 7                              # GDN_ERR_WORKSPACE_TOO_SMALL
     assert call(d_k=64) == 3                             # chunked needs d_k = 128
     assert call(dtype=0) == 4                            # and bf16
@@ -115,8 +115,8 @@ def test_workspace_and_crossover_queries(lib):
     assert ws(4, 1000, 2) == 0 and ws(4, 1000, 0) == 0   # averaging 250 tokens: fused
     assert ws(4, 1000, 4) > 0                            # unless the two kernels are forced
     assert ws(4, 2048, 2) == ws(4, 2048, 4) > 0
-    # header (1 KB-rounded) + (T/64 + N + 1) per-chunk packages of 33 KB per value head
-    assert ws(4, 2048, 4) == 1024 + (2048 // 64 + 5) * 32 * 33792
+    # header (1 KB-rounded) + (T/64 + N + 1) per-chunk packages of 41 KB per value head
+    assert ws(4, 2048, 4) == 1024 + (2048 // 64 + 5) * 32 * 41984
     x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
     assert x > 0
     assert lib.gdn_prefill_crossover_tokens(16, 32, 128, 48, 1) == 2**31 - 1
