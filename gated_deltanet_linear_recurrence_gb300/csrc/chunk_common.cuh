@@ -135,15 +135,18 @@ __device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt,
     store_16x8(MF + o1 * kLdM + o0 + 8 * nt, kLdM, c, -1.f, lane);
   }
   tc::named_sync(kBar, kCount);
-  {  // level 3: Y = A_BL T_TL (32x32x32); warp pw: rows 16 (pw>>2), columns 8 (pw&3)
-    const int mt = pw >> 2, nt = pw & 3;
+  // level 3, eight 16x8 tiles (rows 16 (tile >> 2), columns 8 (tile & 3)) over the warps
+  constexpr int kWarps = (int)(kCount / 32);
+  static_assert(kWarps >= 4 && 8 % kWarps == 0, "the solve runs on 4 or 8 warps");
+  for (int tile = pw; tile < 8; tile += kWarps) {  // Y = A_BL T_TL (32x32x32)
+    const int mt = tile >> 2, nt = tile & 3;
     float c[4];
     warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM, kLdM, MF + 8 * nt, kLdM, lane);
     store_16x8(YF + (16 * mt) * kLdY + 8 * nt, kLdY, c, 1.f, lane);
   }
   tc::named_sync(kBar, kCount);
-  {  // T_BL = -T_BR Y
-    const int mt = pw >> 2, nt = pw & 3;
+  for (int tile = pw; tile < 8; tile += kWarps) {  // T_BL = -T_BR Y
+    const int mt = tile >> 2, nt = tile & 3;
     float c[4];
     warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM + 32, kLdM, YF + 8 * nt, kLdY, lane);
     store_16x8(MF + (32 + 16 * mt) * kLdM + 8 * nt, kLdM, c, -1.f, lane);

@@ -150,51 +150,40 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
       : "memory");
 }
-// shared -> global (16-byte aligned addresses, size a multiple of 16)
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(dst)),
-               "r"(tc::smem_u32(src)), "r"(bytes)
-               : "memory");
-}
-// Wait until every bulk copy this thread issued has read its shared-memory
-// source (the writes complete before the grid does).
-__device__ __forceinline__ void bulk_commit_and_wait_read() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-
 // ------------------------------------------------------------------ prepare
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;  // 4 warps; 4 CTAs per SM (TMEM, registers, shared memory)
 constexpr uint32_t kBarAll = 1, kBarGateP = 2;
-// shared memory of the prepare kernel
-constexpr uint32_t PP_KQ = 0;                      // per d_k half: [Q 8K][K 8K]
-constexpr uint32_t PP_V = 32768;                   // V, two 64-column boxes [t][64], SW128
-constexpr uint32_t PP_TB = PP_V + 16384;           // T diag(b Gamma) bf16, SW128 (solve scratch first)
-constexpr uint32_t PP_TA = PP_TB + 8192;           // T diag(b) bf16, SW128
-constexpr uint32_t PP_MF = PP_TA + 8192;           // A, then T: fp32 [64][kLdM]
-// gates: Gamma[64], decay[64], Gamma_n (+pad) — the package's gates block as
-// laid out in the workspace — then gamma[64], beta[64]
+// Shared memory of the prepare kernel, reused as the item advances:
+//   [0, 32K)     per d_k half kb: [Q 8K][K 8K] (TMA); after G: Q1 holds the
+//                solve scratch, then T diag(b Gamma); after W: K holds V (TMA)
+//   [32K, 49K)   A, then T: fp32 [64][kLdM]; then T diag(b) (bf16) at its start
+//   gates        Gamma[64], decay[64], Gamma_n, then gamma[64], beta[64]
+constexpr uint32_t PP_KQ = 0;
+constexpr uint32_t PP_Q1 = 16384;                  // solve scratch, then T diag(b Gamma)
+constexpr uint32_t PP_V = 8192;                    // V halves over K0 and K1 (stride 16K)
+constexpr uint32_t PP_MF = 32768;
+constexpr uint32_t PP_TA = PP_MF;                  // T diag(b), once T is in registers
 constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;
 constexpr uint32_t PP_MISC = PP_GATE + 5 * 64 * 4;
 constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
-constexpr uint32_t kPrepTmemCols = 256;  // G (cols 0-63), then W (0-127) and U~ (128-255)
+static_assert(4 * (kPrepSmem + 1024) <= 233472, "four prepare CTAs per SM");
+constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W, then U~ (0-127)
 constexpr uint32_t IDP_G = tc::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDP_W = tc::idesc_bf16_f32(64, 128, false, true);
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 4)
     chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31, sp = pw & 3;
+  const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31;
   const int64_t item = blockIdx.x;
   const int64_t cid = item / p.h_v;
   const int h = (int)(item % p.h_v);
   // The chain kernel may launch once every CTA of this grid has started; its
-  // CTAs need an SM without a prepare CTA, so they start as this grid drains.
+  // CTAs need an SM with room, so they start as this grid drains.
   allow_dependents();
   wait_prerequisites();  // the chunk table of the plan kernel
   const int32_t total_chunks = p.chunk_base[p.num_seqs];
@@ -213,7 +202,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   uint8_t* pkg = p.packages + item * (int64_t)kPkgBytes;
 
   float* MF = reinterpret_cast<float*>(smem + PP_MF);
-  float* YF = reinterpret_cast<float*>(smem + PP_TB);
+  float* YF = reinterpret_cast<float*>(smem + PP_Q1);
   float* gsm = reinterpret_cast<float*>(smem + PP_GATE);
   float *Gam = gsm, *dec = gsm + 64, *gam = gsm + 192, *bet = gsm + 256;
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);  // Q, K
@@ -221,6 +210,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   uint64_t* bar_v = bar_tma + 2;                                     // V (needed only for U~)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 3);
   const uint32_t sbase = tc::smem_u32(smem);
+  const int32_t y = static_cast<int32_t>(t0);
 
   if (pw == 0) {
     tc::tmem_alloc(tmem_slot, kPrepTmemCols);
@@ -232,16 +222,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc::mbar_init(bar_v, 1);
     tc::fence_mbar_init();
     tc::mbar_arrive_expect_tx(bar_tma, 32768);
-    tc::mbar_arrive_expect_tx(bar_v, 16384);
-    const int32_t y = static_cast<int32_t>(t0);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
       tc::tma_load_2d(smem + PP_KQ + kb * 16384, &tm_q, hk * kDK + 64 * kb, y, bar_tma);
       tc::tma_load_2d(smem + PP_KQ + kb * 16384 + 8192, &tm_k, hk * kDK + 64 * kb, y, bar_tma);
-      // columns past this head's d_v (d_v < 128) belong to the next head or
-      // lie outside the tensor (zero fill); the slices built from them are
-      // never written
-      tc::tma_load_2d(smem + PP_V + kb * 8192, &tm_v, h * p.d_v + 64 * kb, y, bar_v);
     }
   }
   float gr = 0.f, br = 0.f;
@@ -253,7 +237,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+  const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
   bool ok = tc::mbar_wait(bar_tma, 0);
   tc::fence_after_sync();
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
@@ -272,8 +256,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       float x = gr;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(kFullMask, x, off);
-        if (lane >= off) x += y;
+        const float yv = __shfl_up_sync(kFullMask, x, off);
+        if (lane >= off) x += yv;
       }
       if (pt == 31) MF[0] = x;
       tc::named_sync(kBarGateP, 64);
@@ -283,48 +267,53 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       bet[pt] = br;
       tc::named_sync(kBarGateP, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
-      if (pt == 0) gsm[128] = Gam[kC - 1];
+      float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
+      gout[pt] = Gam[pt];
+      gout[64 + pt] = dec[pt];
+      if (pt == 0) gout[128] = Gam[kC - 1];
     }
     ok = tc::mbar_wait(bar_mma, 0);
     tc::fence_after_sync();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
   }
   if (ok) {
-    // masks: P rows (subpartitions 0,1) over Q's first half (dead once G is
-    // done) in the package's layout, A rows (2,3) to MF
-    const int half = pw >> 2, i0 = 32 * half;
-    float a[32];
-    tc::tmem_ld32(tmem + lane_base + 32 * half, a);
-    if (sp < 2) {
-      const int r = 32 * sp + lane;
-      const float g_r = gam[r];
+    // masks, one G row per thread (TMEM lane pt): P rows (warps 0, 1) to the
+    // package, A rows (warps 2, 3) to MF; 32 columns at a time
+    const int r = 32 * (pw & 1) + lane;
+    const float g_r = gam[r], b_r = bet[r];
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int i0 = 32 * half;
+      float a[32];
+      tc::tmem_ld32(tmem + lane_base + i0, a);
+      if (pw < 2) {
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-        const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+          const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = 4 * e4 + q, i = i0 + e;
-          a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] : 0.f;
+          for (int q = 0; q < 4; ++q) {
+            const int e = 4 * e4 + q, i = i0 + e;
+            a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] : 0.f;
+          }
         }
-      }
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) st_chunk<3>(smem + PP_KQ, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
-    } else {
-      const int r = 32 * (sp - 2) + lane;
-      const float g_r = gam[r], b_r = bet[r];
+        for (int c8 = 0; c8 < 4; ++c8)
+          st_chunk<3>(pkg + kPkgP, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+      } else {
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-        const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
-        float o4[4];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+          const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+          float o4[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = i0 + 4 * e4 + q;
-          o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] : 0.f;
+          for (int q = 0; q < 4; ++q) {
+            const int i = i0 + 4 * e4 + q;
+            o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] : 0.f;
+          }
+          *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
+              make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
-        *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
-            make_float4(o4[0], o4[1], o4[2], o4[3]);
       }
     }
     tc::fence_before_sync();
@@ -333,84 +322,101 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
     unit_lower_inverse<kBarAll, kPrepThreads>(MF, YF, pt, lane);
 
-    {  // T diag(b Gamma) and T diag(b) to shared memory (W and U~ operands)
-      const int r = pt >> 2, q = pt & 3;
+    {  // T diag(b Gamma) over Q1 (W operand), T diag(b) over the start of MF (U~ operand)
+      const int rr = pt >> 1, q = pt & 1;  // row rr, columns 32 q .. 32 q + 31
+      float t[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 2; ++c8) {
-        const int ii = 16 * q + 8 * c8;
-        const float4 m0 = *reinterpret_cast<const float4*>(MF + r * kLdM + ii);
-        const float4 m1 = *reinterpret_cast<const float4*>(MF + r * kLdM + ii + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(bet + ii);
-        const float4 b1 = *reinterpret_cast<const float4*>(bet + ii + 4);
-        const float4 G0 = *reinterpret_cast<const float4*>(Gam + ii);
-        const float4 G1 = *reinterpret_cast<const float4*>(Gam + ii + 4);
-        float xa[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
-                       m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
-        float xb[8] = {xa[0] * G0.x, xa[1] * G0.y, xa[2] * G0.z, xa[3] * G0.w,
-                       xa[4] * G1.x, xa[5] * G1.y, xa[6] * G1.z, xa[7] * G1.w};
-        st_chunk<3>(smem + PP_TA, r * 128 + (2 * q + c8) * 16, xa);
-        st_chunk<3>(smem + PP_TB, r * 128 + (2 * q + c8) * 16, xb);
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 m = *reinterpret_cast<const float4*>(MF + rr * kLdM + 32 * q + 4 * e4);
+        t[4 * e4] = m.x; t[4 * e4 + 1] = m.y; t[4 * e4 + 2] = m.z; t[4 * e4 + 3] = m.w;
+      }
+      tc::named_sync(kBarAll, kPrepThreads);  // every row of T is read before TA overwrites MF
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const int ii = 32 * q + 8 * c8;
+        float xa[8], xb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xa[e] = t[8 * c8 + e] * bet[ii + e];
+          xb[e] = xa[e] * Gam[ii + e];
+        }
+        st_chunk<3>(smem + PP_TA, rr * 128 + (4 * q + c8) * 16, xa);
+        st_chunk<3>(smem + PP_Q1, rr * 128 + (4 * q + c8) * 16, xb);
       }
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
     tc::named_sync(kBarAll, kPrepThreads);
     tc::fence_after_sync();
-    if (pt == 64 && tc::mbar_wait(bar_v, 0)) {  // (on a timeout nothing commits: all time out)
-      tc::fence_after_sync();
+    if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
-        tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_TB + kk * 32, 16, 1024, tc::kLayoutSw128),
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_Q1 + kk * 32, 16, 1024, tc::kLayoutSw128),
                      tc::smem_desc(sbase + PP_KQ + 8192 + kk * 2048, 16384, 1024, tc::kLayoutSw128),
                      IDP_W, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V: M=64 N=128 K=64
-        tc::mma_bf16(tmem + 128, tc::smem_desc(sbase + PP_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
-                     tc::smem_desc(sbase + PP_V + kk * 2048, 8192, 1024, tc::kLayoutSw128), IDP_W,
-                     kk > 0);
       tc::mma_commit(bar_mma);
     }
     ok = tc::mbar_wait(bar_mma, 1);
     tc::fence_after_sync();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (ok) {  // -W over K, U~ over V (M=64 accumulators: row 16 sp + lane on lanes 0-15)
-      const int r = 16 * sp + lane;
-      float w[32];
+  }
+  if (ok) {
+    if (pt == 0) {  // K is consumed: V (two 64-column boxes) over K0 and K1
+      tc::mbar_arrive_expect_tx(bar_v, 16384);
+      // columns past this head's d_v (d_v < 128) belong to the next head or
+      // lie outside the tensor (zero fill); the slices built from them are
+      // never written
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        tc::tmem_ld32(tmem + lane_base + 64 * half + 32 * q2, w);
-        if (lane < 16) {
+      for (int kb = 0; kb < 2; ++kb)
+        tc::tma_load_2d(smem + PP_V + kb * 16384, &tm_v, h * p.d_v + 64 * kb, y, bar_v);
+    }
+    // -W (M=64 accumulator: row 16 w + lane on lanes 0-15) to the package
+    const int r = 16 * pw + lane;
+    float w[32];
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      tc::tmem_ld32(tmem + lane_base + 32 * q4, w);
+      if (lane < 16) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = -w[e];
+        for (int e = 0; e < 32; ++e) w[e] = -w[e];
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            st_chunk<3>(smem + PP_KQ + half * 16384 + 8192, r * 128 + (4 * q2 + c8) * 16,
-                        w + 8 * c8);
-        }
-        tc::tmem_ld32(tmem + lane_base + 128 + 64 * half + 32 * q2, w);
-        const int sl = 2 * half + q2;  // 32-wide slice of d_v
+        for (int c8 = 0; c8 < 4; ++c8)
+          st_chunk<3>(pkg + kPkgW + (q4 >> 1) * 8192, r * 128 + (4 * (q4 & 1) + c8) * 16,
+                      w + 8 * c8);
+      }
+    }
+    tc::fence_before_sync();
+    tc::named_sync(kBarAll, kPrepThreads);  // W's columns are read before U~ overwrites them
+    tc::fence_after_sync();
+    if (pt == 64 && tc::mbar_wait(bar_v, 0)) {  // (on a timeout nothing commits: all time out)
+      tc::fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V: M=64 N=128 K=64
+        tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
+                     tc::smem_desc(sbase + PP_V + kk * 2048, 16384, 1024, tc::kLayoutSw128), IDP_W,
+                     kk > 0);
+      tc::mma_commit(bar_mma);
+    }
+    ok = tc::mbar_wait(bar_mma, 0);
+    tc::fence_after_sync();
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (ok) {  // U~ slices (bf16, 64-byte rows with the SW64 XOR pattern) to the package
+#pragma unroll 1
+      for (int sl = 0; sl < 4; ++sl) {
+        tc::tmem_ld32(tmem + lane_base + 32 * sl, w);
         if (lane < 16 && sl * kDVS < p.d_v) {
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8)
-            st_chunk<2>(smem + PP_V + sl * kPkgUSlice, r * 64 + c8 * 16, w + 8 * c8);
+            st_chunk<2>(pkg + kPkgU + sl * kPkgUSlice, r * 64 + c8 * 16, w + 8 * c8);
         }
       }
     }
-    tc::fence_proxy_async();  // staged package -> bulk copies
   }
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (pw == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
-  if (ok && pt == 0) {  // the package, in four coalesced bulk copies
-    bulk_s2g(pkg + kPkgW, smem + PP_KQ + 8192, 8192);
-    bulk_s2g(pkg + kPkgW + 8192, smem + PP_KQ + 16384 + 8192, 8192);
-    bulk_s2g(pkg + kPkgP, smem + PP_KQ, 8192);
-    bulk_s2g(pkg + kPkgU, smem + PP_V, (uint32_t)(p.d_v / kDVS) * kPkgUSlice);
-    bulk_s2g(pkg + kPkgGates, smem + PP_GATE, 1024);
-    bulk_commit_and_wait_read();  // the CTA's shared memory stays until it is read
-  }
 }
 
 // ------------------------------------------------------------------ chain
