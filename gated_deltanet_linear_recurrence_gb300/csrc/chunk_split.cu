@@ -545,51 +545,56 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    // One thread issues every tensor-core product, in the order the chain needs
-    // them; issuing blocks while the tensor pipe is busy, so no epilogue work
-    // waits behind it.  (Measured on GB300: issuing from lane 0 of this warp is
-    // faster here than issuing from a converged warp under elect.sync.)  Per
-    // chunk c:  [stage landed, state staged] D(c) -> [U staged] S update(c) -> P U(c)
-    if (lane == 0) {
-      // Operand descriptors built once; a stage or K step only adds its byte
-      // offset / 16 to the start-address field (every address is below 256 KB).
-      const uint64_t dSS = tc::smem_desc(sbase + CC_SS, 4096, 512, tc::kLayoutSw64);
-      const uint64_t dUK = tc::smem_desc(sbase + CC_UK, 4096, 512, tc::kLayoutSw64);
-      const uint64_t dUB = tc::smem_desc(sbase + CC_UB, 4096, 512, tc::kLayoutSw64);
-      const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
-      const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
-      const uint64_t dP0 = tc::smem_desc(sbase + CC_TAIL + TL_P - 8192, 16, 1024, tc::kLayoutSw128);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c % kStages;
-        const uint64_t so = (uint64_t)((st * kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
-        const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
-        const uint32_t td = tmem + TC_D0 + 32 * (c & 1), to2 = tmem + TC_O0 + 32 * (c & 1);
-        ok = tc::mbar_wait(&full[st], (c / kStages) & 1);
-        if (!ok) break;
-        ok = tc::mbar_wait(bar_ss, c & 1);
-        if (!ok) break;
-        tc::fence_after_sync();
+    // Issues every tensor-core product, in the order the chain needs them.  The
+    // whole warp runs the loop converged: every lane waits on the barrier
+    // itself, and one elected lane issues the MMAs and commits.  (Measured on
+    // GB300, this issues ~10 % faster per call than a loop that only lane 0
+    // runs, and much faster than lane 0 waiting and broadcasting by shuffle.)
+    // Per chunk c:  [stage landed, state staged] D(c) -> [U staged] S update(c) -> P U(c)
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool w = tc::mbar_wait(bar, parity);
+      tc::fence_after_sync();
+      return __all_sync(kFullMask, w) != 0;
+    };
+    // Operand descriptors built once; a stage or K step only adds its byte
+    // offset / 16 to the start-address field (every address is below 256 KB).
+    const uint64_t dSS = tc::smem_desc(sbase + CC_SS, 4096, 512, tc::kLayoutSw64);
+    const uint64_t dUK = tc::smem_desc(sbase + CC_UK, 4096, 512, tc::kLayoutSw64);
+    const uint64_t dUB = tc::smem_desc(sbase + CC_UB, 4096, 512, tc::kLayoutSw64);
+    const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
+    const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
+    const uint64_t dP0 = tc::smem_desc(sbase + CC_TAIL + TL_P - 8192, 16, 1024, tc::kLayoutSw128);
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c % kStages;
+      const uint64_t so = (uint64_t)((st * kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
+      const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
+      const uint32_t td = tmem + TC_D0 + 32 * (c & 1), to2 = tmem + TC_O0 + 32 * (c & 1);
+      if (!(ok = warp_wait(&full[st], (c / kStages) & 1) && warp_wait(bar_ss, c & 1))) break;
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // D = [-W; Q] S_s^T
-          tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4), dSS + ((kk * 1024) >> 4),
-                       IDC_WQ, kk > 0);
+          tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
+                       dSS + ((kk * 1024) >> 4), IDC_WQ, kk > 0);
         tc::mma_commit(bar_d);
-        ok = tc::mbar_wait(bar_u, c & 1);
-        if (!ok) break;
-        tc::fence_after_sync();
+      }
+      __syncwarp();
+      if (!(ok = warp_wait(bar_u, c & 1))) break;
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
           tc::mma_bf16(tmem + TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4), IDC_SU, 1);
         tc::mma_commit(bar_s);
         tc::mma_commit(&empty[st]);  // -W, Q, K and U~ of the stage consumed
-        ok = tc::mbar_wait(&tfull[st], (c / kStages) & 1);
-        if (!ok) break;
-        tc::fence_after_sync();
+      }
+      __syncwarp();
+      if (!(ok = warp_wait(&tfull[st], (c / kStages) & 1))) break;
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
           tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), IDC_PU, kk > 0);
         tc::mma_commit(&bar_o[c & 1]);
       }
+      __syncwarp();
     }
   } else {
     // Epilogue warps.  Warps 0-1 (TMEM lanes 0-63) form U; warps 2-3 (lanes
