@@ -39,14 +39,16 @@ FP32_LANES_PER_SM = 128
 # kernel's sources hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh",
-                              "params.h"],
-                    "sha256_16": "unmeasured", "bytes": None,
+                              "params.h", "per_device.h"],
+                    "sha256_16": "53daa5d735b0ef87",
+                    "bytes": 5_120 + (68_248_320 + 31_823_104) + (119_582_464 + 15_531_264),
                     "profile": "profiles/chunk_split_t4096.md"},
-    "chunk_prefill": {"files": ["chunk_prefill.cu", "tc.cuh", "rows.cuh", "params.h"],
+    "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh",
+                                "params.h", "per_device.h"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "params.h"],
-                    "sha256_16": "bdc6d4c3a147886a", "bytes": 541_162_496 + 479_516_672,
+                    "sha256_16": "be6471840ce4ac6c", "bytes": 541_181_952 + 479_234_560,
                     "profile": "profiles/decode_step_b256.md"},
 }
 

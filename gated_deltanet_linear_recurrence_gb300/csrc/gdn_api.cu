@@ -52,11 +52,11 @@ gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
 constexpr int32_t kCrossoverTokens = 16;
 
 // Fused vs two-kernel chunked evaluation.  Same sweep: the fused kernel is
-// faster up to 384 tokens (31.4 vs 33.4 us), the two kernels from 512 tokens
-// (35.5 vs 39.6 us; 4.30 vs 7.80 ms at 128K tokens).  GDN_ALGO_AUTO and
+// faster up to 128 tokens (17.1 vs 20.1 us), the two kernels from 256 tokens
+// (23.2 vs 25.2 us; 3.20 vs 7.83 ms at 128K tokens).  GDN_ALGO_AUTO and
 // GDN_ALGO_CHUNKED use the two kernels when the sequences average at least
 // this many tokens and the caller's workspace is large enough.
-constexpr int64_t kSplitMinAvgTokens = 512;
+constexpr int64_t kSplitMinAvgTokens = 256;
 
 bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
   return num_seqs > 0 && total_tokens >= kSplitMinAvgTokens * num_seqs;

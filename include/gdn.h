@@ -99,7 +99,7 @@ typedef enum {
  * either as one fused kernel that needs no workspace, or as two kernels (the
  * per-chunk state-independent work spread over all SMs, then the sequential
  * state pass) that meet in the workspace.  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED
- * take the two kernels when the sequences average at least 512 tokens (where
+ * take the two kernels when the sequences average at least 256 tokens (where
  * they measured faster on GB300) and workspace_bytes is at least
  * gdn_prefill_workspace_size(...), else the fused kernel;
  * GDN_ALGO_CHUNKED_SPLIT always takes them and returns GDN_ERR_NULL_POINTER or

@@ -208,13 +208,13 @@ def test_fused_and_two_kernel_forms_agree(lengths):
 
 def test_library_choice_of_chunked_form():
     """algo='chunked' takes the two kernels (bitwise) only for sequences averaging
-    512 tokens or more; shorter ones take the fused kernel and need no workspace."""
+    256 tokens or more; shorter ones take the fused kernel and need no workspace."""
     from gated_deltanet_linear_recurrence_gb300 import gdn_prefill_workspace_size as wss
-    assert wss(2, 1000, 2, 4, 128, 64, algo="chunked") == 0
-    assert wss(2, 1000, 2, 4, 128, 64, algo="chunked_split") > 0
-    assert wss(2, 1024, 2, 4, 128, 64, algo="chunked") > 0
+    assert wss(2, 500, 2, 4, 128, 64, algo="chunked") == 0
+    assert wss(2, 500, 2, 4, 128, 64, algo="chunked_split") > 0
+    assert wss(2, 512, 2, 4, 128, 64, algo="chunked") > 0
     assert wss(1, 4096, 2, 4, 128, 64, algo="chunked_fused") == 0
-    for lengths, form in (([500, 500], "chunked_fused"), ([600, 424], "chunked_split")):
+    for lengths, form in (([250, 250], "chunked_fused"), ([300, 212], "chunked_split")):
         d = inputs.make_prefill(lengths, 2, 4, 128, 64, "bf16", seed=23, state_std=0.05)
         o, st = run(d, algo="chunked")
         o2, st2 = run(d, algo=form)
