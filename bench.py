@@ -244,6 +244,9 @@ def main():
                     help="time the token scan and the chunked prefill over sequence lengths "
                          "(one sequence, 16 key / 32 value heads of 128, bf16) and print the "
                          "crossover table as JSON lines")
+    ap.add_argument("--stream", action="store_true",
+                    help="time the 128K-token prompt as one call and as streamed pieces "
+                         "(gdn_prefill_streamed), with the workspace each needs, as JSON lines")
     ap.add_argument("--kernel-only", choices=["prefill", "decode_b256"], default=None,
                     help="run only this kernel's workload (warmup + steps launches, no JSON); "
                          "for profiler captures")
@@ -256,6 +259,8 @@ def main():
         return run_kernel_only(args)
     if args.sweep:
         return run_sweep(args)
+    if args.stream:
+        return run_stream(args)
 
     import torch
     import torch.distributed as dist
@@ -542,6 +547,54 @@ def run_sweep(args):
                   if min(r["chunked_us"], r["chunked_fused_us"]) < r["scan_us"]), None)
     split = next((r["T"] for r in rows if r["chunked_us"] < r["chunked_fused_us"]), None)
     print(json.dumps({"crossover_tokens": cross, "split_from_tokens": split}), flush=True)
+
+
+def run_stream(args):
+    """The 128K-token prompt: one gdn_prefill call against gdn_prefill_streamed with
+    pieces of several sizes (CUDA events, L2 flushed before each call)."""
+    import torch
+    from gated_deltanet_linear_recurrence_gb300 import (gdn_prefill, gdn_prefill_streamed,
+                                                        gdn_prefill_streamed_workspace_size,
+                                                        gdn_prefill_workspace_size,
+                                                        gdn_stream_status, inputs)
+
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    w = inputs.WORKLOADS["prefill_t131072"]
+    d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                            seed=w["seed"], state_std=w["state_std"])
+    x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    T = sum(w["lengths"])
+    o = torch.empty((T, w["h_v"], w["d_v"]), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((1, w["h_v"], w["d_v"], w["d_k"]), dtype=torch.float32, device=dev)
+    shape = (w["h_k"], w["h_v"], w["d_k"], w["d_v"])
+    cases = [("whole", None, gdn_prefill_workspace_size(1, T, *shape, algo="chunked_split"))]
+    for piece in (2048, 8192, 32768):
+        cases.append((f"pieces of {piece}", piece,
+                      gdn_prefill_streamed_workspace_size(piece, *shape)))
+    for name, piece, ws_bytes in cases:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        ts = []
+        for i in range(args.warmup + 5):
+            flush_buf.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            if piece is None:
+                gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                            state_in=x["state_in"], state_out=st, o=o, algo="chunked_split",
+                            workspace=ws)
+            else:
+                gdn_prefill_streamed(x["q"], x["k"], x["v"], x["g"], x["beta"], piece,
+                                     state_in=x["state_in"], state_out=st, o=o, workspace=ws)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ts.append(a.elapsed_time(b) * 1e3)
+        assert gdn_stream_status() == "GDN_OK"
+        us = statistics.median(ts)
+        print(json.dumps({"case": name, "tokens": T, "us": us, "tok_s": T / (us / 1e6),
+                          "workspace_bytes": ws_bytes}), flush=True)
+        del ws
 
 
 def run_kernel_only(args):

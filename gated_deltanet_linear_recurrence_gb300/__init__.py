@@ -12,7 +12,8 @@ import torch
 from . import _lib
 from ._lib import GdnError, STATUS_NAMES
 
-__all__ = ["gdn_prefill", "gdn_prefill_noalloc", "gdn_decode_step", "gdn_prefill_workspace_size",
+__all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
+           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
@@ -94,6 +95,43 @@ def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=N
                          dt, float(scale), _lib.ALGOS[algo], _ptr(workspace), ws_bytes,
                          _stream(stream))
     _lib.check(st, "gdn_prefill")
+    return o, state_out
+
+
+def gdn_prefill_streamed_workspace_size(piece_tokens, h_k, h_v, d_k, d_v, dtype=torch.bfloat16):
+    return int(_lib.load().gdn_prefill_streamed_workspace_size(piece_tokens, h_k, h_v, d_k, d_v,
+                                                               _DTYPES[dtype]))
+
+
+def gdn_prefill_streamed(q, k, v, g, beta, piece_tokens, state_in=None, state_out=None, o=None,
+                         scale=1.0, workspace=None, stream=None):
+    """One sequence (q, k [T, h_k, d_k]; v [T, h_v, d_v]; g, beta [T, h_v]) prefilled
+    as pieces of ``piece_tokens`` tokens (a multiple of 64) with the state carried
+    between them (gdn_prefill_streamed in include/gdn.h).  Returns (o, state_out
+    [1, h_v, d_v, d_k]); a workspace of gdn_prefill_streamed_workspace_size() bytes
+    is allocated when none is given (its size does not depend on T)."""
+    lib = _lib.load()
+    T, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    _require(k.shape == q.shape and v.shape[0] == T, "q/k/v shapes disagree")
+    _require(g.shape == (T, h_v) and beta.shape == (T, h_v), "g/beta must be [T, h_v]")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    for t in (q, k, v, g, beta):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((T, h_v, d_v), dtype=q.dtype, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((1, h_v, d_v, d_k), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = lib.gdn_prefill_streamed_workspace_size(piece_tokens, h_k, h_v, d_k, d_v, dt)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_prefill_streamed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                                  _ptr(state_out), _ptr(o), T, h_k, h_v, d_k, d_v, dt,
+                                  float(scale), int(piece_tokens), _ptr(workspace), ws_bytes,
+                                  _stream(stream))
+    _lib.check(st, "gdn_prefill_streamed")
     return o, state_out
 
 

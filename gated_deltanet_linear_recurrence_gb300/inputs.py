@@ -46,6 +46,8 @@ def _draw_qk(gen, tokens, heads, dim, dtype):
 
 def _draw_normal(gen, shape, dtype, std=1.0):
     out = torch.empty(shape, dtype=dtype)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1)
     for t0 in range(0, shape[0], _BLOCK_TOKENS):
         t1 = min(shape[0], t0 + _BLOCK_TOKENS)

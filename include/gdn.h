@@ -122,6 +122,37 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
                                   gdn_algo algo);
 
 /*
+ * gdn_prefill_streamed — one sequence of total_tokens tokens prefilled as
+ * consecutive pieces of piece_tokens tokens (a positive multiple of 64; the
+ * last piece may be shorter), the state carried from piece to piece in
+ * state_out.  Page "Optimizing on-device inference for Apple Silicon", section
+ * "Limit scratch memory by splitting prompts into chunks": a long prompt runs
+ * as bounded pieces whose recurrent state carries the context, so the scratch
+ * memory is bounded by the piece, not the prompt.
+ *
+ * Same tensors as gdn_prefill for one sequence (no cu_seqlens: the sequence is
+ * tokens 0 .. total_tokens-1); state_in may be NULL (zeros) or equal state_out.
+ * Every piece runs the two-kernel chunked evaluation (bf16, d_k 128, d_v a
+ * multiple of 32), else the token scan, so the result equals bit for bit
+ * gdn_prefill with GDN_ALGO_CHUNKED_SPLIT (resp. GDN_ALGO_SCAN) on the whole
+ * sequence.  workspace: required, 16-byte aligned, at least
+ * gdn_prefill_streamed_workspace_size(piece_tokens, ...) bytes, which does not
+ * depend on total_tokens.  Errors: GDN_ERR_INVALID_ARG for a bad piece size,
+ * GDN_ERR_WORKSPACE_TOO_SMALL, and those of gdn_prefill.
+ */
+gdn_status gdn_prefill_streamed(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* state_in, float* state_out,
+                                void* o, int64_t total_tokens, int32_t h_k, int32_t h_v,
+                                int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
+                                int64_t piece_tokens, void* workspace, size_t workspace_bytes,
+                                gdn_stream_t stream);
+
+/* Workspace bytes for gdn_prefill_streamed with pieces of piece_tokens tokens
+ * (0 for an invalid piece size or head shape). */
+size_t gdn_prefill_streamed_workspace_size(int64_t piece_tokens, int32_t h_k, int32_t h_v,
+                                           int32_t d_k, int32_t d_v, gdn_dtype dtype);
+
+/*
  * gdn_prefill_noalloc — gdn_prefill with GDN_ALGO_CHUNKED_SPLIT (the
  * two-kernel chunked evaluation), taking its scratch from a fixed array of
  * GDN_NOALLOC_SCRATCH_BYTES that the library holds in device memory instead of

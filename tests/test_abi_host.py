@@ -120,3 +120,33 @@ def test_workspace_and_crossover_queries(lib):
     x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
     assert x > 0
     assert lib.gdn_prefill_crossover_tokens(16, 32, 128, 48, 1) == 2**31 - 1
+
+
+def test_streamed_host_errors(lib):
+    """gdn_prefill_streamed refuses bad arguments before launching anything."""
+    def call(t=4096, piece=1024, h_k=16, h_v=32, d_k=128, d_v=128, dtype=1, ws=FAKE,
+             ws_bytes=1 << 40, **ptr):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=None, state_out=FAKE, o=FAKE)
+        p.update(ptr)
+        return lib.gdn_prefill_streamed(p["q"], p["k"], p["v"], p["g"], p["beta"], p["state_in"],
+                                        p["state_out"], p["o"], t, h_k, h_v, d_k, d_v, dtype, 1.0,
+                                        piece, ws, ws_bytes, None)
+    assert call(piece=1000) == 2                         # not whole chunks
+    assert call(piece=0) == 2
+    assert call(t=-1) == 2
+    assert call(d_k=48) == 3
+    assert call(h_k=3, h_v=4) == 3
+    assert call(q=None) == 1
+    assert call(ws=None) == 1
+    assert call(ws=FAKE + 8) == 5
+    assert call(k=FAKE + 4) == 5
+    assert call(ws_bytes=4096) == 7                      # GDN_ERR_WORKSPACE_TOO_SMALL
+    assert call(state_in=FAKE + 64) == 2                 # partial overlap with state_out
+    size = lib.gdn_prefill_streamed_workspace_size
+    assert size(1000, 16, 32, 128, 128, 1) == 0
+    # bounded by the piece: the same for any prompt length, and far below the whole
+    # prompt's workspace for a 128K-token prompt
+    assert size(8192, 16, 32, 128, 128, 1) == 256 + lib.gdn_prefill_workspace_size(
+        1, 8192, 16, 32, 128, 128, 1, 4)
+    assert size(8192, 16, 32, 128, 128, 1) * 10 < lib.gdn_prefill_workspace_size(
+        1, 131072, 16, 32, 128, 128, 1, 4)
