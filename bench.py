@@ -36,19 +36,18 @@ FP32_LANES_PER_SM = 128
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of each kernel (summaries under profiles/), valid only while the
-# kernel's sources hash to the recorded value.
+# kernel's device sources (the .cu and the device headers it includes) hash to
+# the recorded value.
 NCU_TRAFFIC = {
-    "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh",
-                              "params.h", "per_device.h"],
-                    "sha256_16": "53daa5d735b0ef87",
+    "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
+                    "sha256_16": "93d024016f3513fb",
                     "bytes": 5_120 + (68_248_320 + 31_823_104) + (119_582_464 + 15_531_264),
                     "profile": "profiles/chunk_split_t4096.md"},
-    "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh",
-                                "params.h", "per_device.h"],
+    "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
-    "decode_step": {"files": ["decode_step.cu", "rows.cuh", "params.h"],
-                    "sha256_16": "be6471840ce4ac6c", "bytes": 541_181_952 + 479_234_560,
+    "decode_step": {"files": ["decode_step.cu", "rows.cuh"],
+                    "sha256_16": "b48aed3378955542", "bytes": 541_181_952 + 479_234_560,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
@@ -462,7 +461,44 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
     out["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic("decode_step"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
-    del y, o, dd
+
+    # the same 256 sequences advanced by 4 tokens in one launch (gdn_decode_multi),
+    # without and with the per-token state snapshots
+    from gated_deltanet_linear_recurrence_gb300 import gdn_decode_multi
+    n_tok, B = 4, w["batch"]
+    dm = inputs.make_prefill([n_tok] * B, w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
+                             seed=w["seed"] + 7)
+    mm = {k: dm[k].to(dev).reshape(B, n_tok, *dm[k].shape[1:]).contiguous()
+          for k in ("q", "k", "v", "g", "beta")}
+    om = torch.empty((B, n_tok, w["h_v"], w["d_v"]), dtype=torch.bfloat16, device=dev)
+    snap = torch.empty((B, n_tok, w["h_v"], w["d_v"], w["d_k"]), dtype=torch.float32, device=dev)
+    per_token = nbytes - 2 * y["state"].numel() * 4
+    for with_snap in (False, True):
+        def mstep():
+            gdn_decode_multi(mm["q"], mm["k"], mm["v"], mm["g"], mm["beta"], y["state"], o=om,
+                             snapshots=snap if with_snap else False, stream=stream)
+
+        for _ in range(args.warmup):
+            mstep()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            a.record(stream)
+            mstep()
+            b.record(stream)
+        torch.cuda.synchronize()
+        mms = statistics.median([a.elapsed_time(b) for a, b in evs])
+        mbytes = 2 * y["state"].numel() * 4 + n_tok * per_token
+        if with_snap:
+            mbytes += snap.numel() * 4
+        key = "decode_multi_b256_n4" + ("_snapshots" if with_snap else "")
+        out[key] = {"us_per_call": mms * 1e3, "tokens_per_call": B * n_tok,
+                    "tok_s": B * n_tok / (mms / 1e3), "bytes_per_call": mbytes,
+                    "gbs": mbytes / (mms / 1e3) / 1e9,
+                    "frac_of_measured_hbm": mbytes / (mms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "vs_4_single_steps": 4 * ms / mms}
+    del y, o, dd, mm, om, snap, dm
 
     # batch-1 decode through 30 layers: one CUDA graph of 30 calls per step
     w = inputs.WORKLOADS["decode_b1_x30layers"]

@@ -13,7 +13,8 @@ from . import _lib
 from ._lib import GdnError, STATUS_NAMES
 
 __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
-           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_prefill_workspace_size",
+           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi",
+           "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
@@ -182,6 +183,40 @@ def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None):
                              _ptr(o), B, h_k, h_v, d_k, d_v, dt, float(scale), _stream(stream))
     _lib.check(st, "gdn_decode_step")
     return o
+
+
+def gdn_decode_multi(q, k, v, g, beta, state, o=None, snapshots=False, scale=1.0, stream=None):
+    """n tokens for each of B sequences in one launch (gdn_decode_multi in
+    include/gdn.h): q, k [B, n, h_k, d_k]; v [B, n, h_v, d_v]; g, beta [B, n, h_v]
+    fp32; state [B, h_v, d_v, d_k] fp32 updated in place to the state after the
+    last token.  ``snapshots``: False (none), True (allocated and returned) or a
+    [B, n, h_v, d_v, d_k] fp32 tensor receiving the state after each token.
+    Returns o [B, n, h_v, d_v], or (o, snapshots) when snapshots are asked for."""
+    lib = _lib.load()
+    B, n, h_k, d_k = q.shape
+    h_v, d_v = v.shape[2], v.shape[3]
+    _require(k.shape == q.shape and v.shape[:2] == (B, n), "q/k/v shapes disagree")
+    _require(g.shape == (B, n, h_v) and beta.shape == (B, n, h_v), "g/beta must be [B, n, h_v]")
+    _require(state.shape == (B, h_v, d_v, d_k) and state.dtype == torch.float32,
+             "state must be [B, h_v, d_v, d_k] fp32")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    for t in (q, k, v, g, beta, state):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((B, n, h_v, d_v), dtype=q.dtype, device=q.device)
+    snap = None
+    if snapshots is True:
+        snap = torch.empty((B, n, h_v, d_v, d_k), dtype=torch.float32, device=q.device)
+    elif snapshots is not False and snapshots is not None:
+        snap = snapshots
+        _require(snap.shape == (B, n, h_v, d_v, d_k) and snap.dtype == torch.float32 and
+                 snap.is_contiguous(), "snapshots must be [B, n, h_v, d_v, d_k] fp32")
+    st = lib.gdn_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                              _ptr(o), _ptr(snap), B, n, h_k, h_v, d_k, d_v, dt, float(scale),
+                              _stream(stream))
+    _lib.check(st, "gdn_decode_multi")
+    return o if snap is None else (o, snap)
 
 
 def gdn_stream_status(stream=None):

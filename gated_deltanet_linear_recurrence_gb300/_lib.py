@@ -37,6 +37,8 @@ SIGNATURES = {
                                            _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                        _i32, ctypes.c_int, _f32, _vp]),
+    "gdn_decode_multi": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                        _i32, _i32, _i32, ctypes.c_int, _f32, _vp]),
     "gdn_stream_status": (ctypes.c_int, [_vp]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_prefill_crossover_tokens": (_i32, [_i32, _i32, _i32, _i32, ctypes.c_int]),

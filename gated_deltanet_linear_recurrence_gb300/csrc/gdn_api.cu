@@ -207,6 +207,36 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
   return GDN_OK;
 }
 
+gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float* state, void* o, float* snapshots,
+                            int32_t batch, int32_t n_tokens, int32_t h_k, int32_t h_v,
+                            int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
+                            gdn_stream_t stream) {
+  if (batch < 0 || n_tokens < 1 || n_tokens > 1024) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  if (st != GDN_OK) return st;
+  if (batch == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !state || !o) return GDN_ERR_NULL_POINTER;
+  const void* ptrs[] = {q, k, v, g, beta, state, o, snapshots};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  if (snapshots) {  // the snapshots must not overlap the state
+    const size_t state_bytes = (size_t)batch * h_v * d_v * d_k * sizeof(float);
+    const char* a = reinterpret_cast<const char*>(state);
+    const char* b = reinterpret_cast<const char*>(snapshots);
+    if (a < b + state_bytes * n_tokens && b < a + state_bytes) return GDN_ERR_INVALID_ARG;
+  }
+  gdn::DecodeMultiArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.o = o;
+  a.snapshots = snapshots;
+  a.batch = batch; a.n_tokens = n_tokens; a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
+  a.dtype = dtype; a.scale = scale;
+  if (gdn::launch_decode_multi(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
 gdn_status gdn_stream_status(gdn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GDN_ERR_CUDA;

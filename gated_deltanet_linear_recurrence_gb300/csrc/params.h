@@ -25,6 +25,23 @@ struct DecodeArgs {
   float scale;
 };
 
+// Several tokens per sequence: q, k [B][n][h_k][d_k], v, o [B][n][h_v][d_v],
+// g, beta [B][n][h_v]; state [B][h_v][d_v][d_k] in place; snapshots
+// [B][n][h_v][d_v][d_k] (the state after each token) or nullptr.
+struct DecodeMultiArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float* state;
+  void* o;
+  float* snapshots;
+  int32_t batch, n_tokens, h_k, h_v, d_k, d_v;
+  int dtype;
+  float scale;
+};
+
 struct PrefillArgs {
   const void* q;            // [T][h_k][d_k] dtype
   const void* k;            // [T][h_k][d_k] dtype
@@ -50,6 +67,7 @@ struct PrefillArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream);
 size_t chunked_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,

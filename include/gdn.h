@@ -201,6 +201,29 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            gdn_stream_t stream);
 
 /*
+ * gdn_decode_multi — n_tokens (1 .. 1024) consecutive tokens for each of
+ * `batch` sequences in one launch: the state is read once, carried through the
+ * tokens and written once.  Page "Optimizing on-device inference for Apple
+ * Silicon", section "Limits of further optimization": speculative decoding
+ * verifies groups of two to five rows per step; after a rejected draft token
+ * the caller goes back to the state after the last accepted one, which
+ * `snapshots` provides.  The results equal n_tokens successive gdn_decode_step
+ * calls bit for bit.
+ *
+ * q, k [batch][n_tokens][h_k][d_k] and v, o [batch][n_tokens][h_v][d_v] in
+ * `dtype`; g, beta [batch][n_tokens][h_v] fp32; state [batch][h_v][d_v][d_k]
+ * fp32, updated in place to the state after the last token; snapshots NULL or
+ * [batch][n_tokens][h_v][d_v][d_k] fp32 receiving the state after each token
+ * (must not overlap the state).  Same head mapping and scale as
+ * gdn_decode_step.
+ */
+gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float* state, void* o, float* snapshots,
+                            int32_t batch, int32_t n_tokens, int32_t h_k, int32_t h_v,
+                            int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
+                            gdn_stream_t stream);
+
+/*
  * gdn_stream_status — synchronise `stream`, then report (and clear) the
  * current device's error word: GDN_OK, GDN_ERR_BAD_CU_SEQLENS,
  * GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if the stream reported a CUDA error.

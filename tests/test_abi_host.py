@@ -150,3 +150,20 @@ def test_streamed_host_errors(lib):
         1, 8192, 16, 32, 128, 128, 1, 4)
     assert size(8192, 16, 32, 128, 128, 1) * 10 < lib.gdn_prefill_workspace_size(
         1, 131072, 16, 32, 128, 128, 1, 4)
+
+
+def test_decode_multi_host_errors(lib):
+    def call(b=2, n=3, h_k=1, h_v=1, d_k=16, d_v=16, dtype=1, snap=None, **ptr):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE)
+        p.update(ptr)
+        return lib.gdn_decode_multi(p["q"], p["k"], p["v"], p["g"], p["beta"], p["state"], p["o"],
+                                    snap, b, n, h_k, h_v, d_k, d_v, dtype, 1.0, None)
+    assert call(n=0) == 2
+    assert call(n=2000) == 2
+    assert call(b=-1) == 2
+    assert call(d_k=8) == 3
+    assert call(dtype=4) == 4
+    assert call(state=None) == 1
+    assert call(o=FAKE + 2) == 5
+    assert call(snap=FAKE + 16) == 2                     # snapshots overlap the state
+    assert call(b=0) == 0
