@@ -27,11 +27,12 @@ def _lib(mutant=0):
         vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
         lib.gdn_oracle_prefill.restype = ctypes.c_int
         lib.gdn_oracle_prefill.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
-                                           vp, i32, i64, i32, i32, i32, i32, dbl, vp, vp, i32]
+                                           vp, i32, i64, i32, i32, i32, i32, dbl, ctypes.c_int,
+                                           vp, vp, i32]
         lib.gdn_oracle_rows.restype = ctypes.c_int
         lib.gdn_oracle_rows.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
-                                        vp, i32, i64, i32, i32, i32, i32, dbl, vp, i64, vp,
-                                        vp, vp, i32]
+                                        vp, i32, i64, i32, i32, i32, i32, dbl, ctypes.c_int,
+                                        vp, i64, vp, vp, vp, i32]
         lib.gdn_oracle_default_threads.restype = ctypes.c_int
         _libs[mutant] = lib
     return _libs[mutant]
@@ -88,10 +89,11 @@ def _prep(q, k, v, g, beta, state_in, cu_seqlens):
 
 
 def prefill(q, k, v, g, beta, cu_seqlens, h_k, h_v, d_k, d_v, state_in=None, scale=1.0,
-            threads=0, mutant=0):
+            threads=0, mutant=0, qk_l2norm=False):
     """Full evaluation.  Returns (o [T, h_v, d_v] fp64, state [N, h_v, d_v, d_k] fp64).
 
-    Output rows of tokens that belong to no sequence stay NaN.
+    Output rows of tokens that belong to no sequence stay NaN.  ``qk_l2norm``
+    divides q and k of every (token, key head) by sqrt(|x|^2 + 1e-6) first.
     """
     qa, ka, va, ga, ba, sa, cu, qd, gd = _prep(q, k, v, g, beta, state_in, cu_seqlens)
     n = len(cu) - 1
@@ -101,7 +103,8 @@ def prefill(q, k, v, g, beta, cu_seqlens, h_k, h_v, d_k, d_v, state_in=None, sca
     st = np.zeros((n, h_v, d_v, d_k))
     rc = _lib(mutant).gdn_oracle_prefill(qd, gd, _ptr(qa), _ptr(ka), _ptr(va), _ptr(ga),
                                          _ptr(ba), _ptr(sa), _ptr(cu), n, total, h_k, h_v,
-                                         d_k, d_v, float(scale), _ptr(o), _ptr(st), threads)
+                                         d_k, d_v, float(scale), int(bool(qk_l2norm)), _ptr(o),
+                                         _ptr(st), threads)
     if rc:
         raise ValueError(f"oracle: {_ERRORS.get(rc, rc)}")
     del t
@@ -109,7 +112,7 @@ def prefill(q, k, v, g, beta, cu_seqlens, h_k, h_v, d_k, d_v, state_in=None, sca
 
 
 def rows(q, k, v, g, beta, cu_seqlens, h_k, h_v, d_k, d_v, tasks, state_in=None, scale=1.0,
-         threads=0, mutant=0):
+         threads=0, mutant=0, qk_l2norm=False):
     """Sampled evaluation of value rows.
 
     ``tasks`` is a sequence of (seq, value_head, row).  Returns a list with, per
@@ -130,7 +133,8 @@ def rows(q, k, v, g, beta, cu_seqlens, h_k, h_v, d_k, d_v, tasks, state_in=None,
     st = np.zeros((max(len(tk), 1), d_k))
     rc = _lib(mutant).gdn_oracle_rows(qd, gd, _ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba),
                                       _ptr(sa), _ptr(cu), n, total, h_k, h_v, d_k, d_v,
-                                      float(scale), _ptr(tk), len(tk), _ptr(off), _ptr(o),
+                                      float(scale), int(bool(qk_l2norm)), _ptr(tk), len(tk),
+                                      _ptr(off), _ptr(o),
                                       _ptr(st), threads)
     if rc:
         raise ValueError(f"oracle: {_ERRORS.get(rc, rc)}")

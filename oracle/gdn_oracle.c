@@ -38,7 +38,12 @@
  *   - value heads 2j and 2j+1 (generally G*j ... G*j+G-1) share key head j;
  *   - one gate g and one write strength beta per (token, value head);
  *   - an empty sequence leaves its state unchanged and writes no output;
- *   - a NULL initial state means zeros.
+ *   - a NULL initial state means zeros;
+ *   - with qk_l2norm set, q and k of every (token, key head) are first divided
+ *     by sqrt(sum of their squares + 1e-6): the page (section "Reduce
+ *     intermediate and state traffic") fuses the recurrent update with "its
+ *     normalization" without giving its form, and L2 normalisation of q and k
+ *     per head is the plainest reading; eps = 1e-6 is the usual choice.
  *
  * Build: gcc -O2 -std=c11 -shared -fPIC -pthread (see oracle/build.py).
  * ORACLE_MUTANT selects a deliberately wrong variant; only the pin-strength
@@ -56,6 +61,8 @@
 #endif
 
 enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2 };
+
+#define QK_NORM_EPS 1e-6
 
 enum {
   ORC_OK = 0,
@@ -90,6 +97,7 @@ typedef struct {
   int64_t total_tokens;
   int32_t h_k, h_v, d_k, d_v;
   double scale;
+  int qk_l2norm; /* divide q and k by their L2 norm (+ eps) first */
   /* task list: (seq, head, row) triples; NULL means every row of every head */
   const int64_t* tasks;
   int64_t num_tasks;
@@ -144,8 +152,33 @@ static void run_row(const job_t* J, int32_t n, int32_t h, int32_t i, double* sro
     const int64_t gv_off = t * J->h_v + h;
     for (int32_t j = 0; j < dk; ++j) {
       krow[j] = widen(J->k, J->qkv_dtype, qk_off + j);
-      qrow[j] = scale * widen(J->q, J->qkv_dtype, qk_off + j);
+      qrow[j] = widen(J->q, J->qkv_dtype, qk_off + j);
     }
+#if ORACLE_MUTANT == 13
+    if (J->qk_l2norm)
+      for (int32_t j = 0; j < dk; ++j) qrow[j] *= scale;
+#endif
+    if (J->qk_l2norm) { /* k <- k / sqrt(|k|^2 + eps), the same for q */
+      double kss = 0.0, qss = 0.0;
+      for (int32_t j = 0; j < dk; ++j) {
+        kss += krow[j] * krow[j];
+        qss += qrow[j] * qrow[j];
+      }
+      const double kn = 1.0 / sqrt(kss + QK_NORM_EPS), qn = 1.0 / sqrt(qss + QK_NORM_EPS);
+      for (int32_t j = 0; j < dk; ++j) {
+        krow[j] *= kn;
+#if ORACLE_MUTANT != 12 /* q left unnormalised */
+        qrow[j] *= qn;
+#endif
+      }
+#if ORACLE_MUTANT == 12
+      (void)qn;
+#endif
+    }
+#if ORACLE_MUTANT == 13 /* scale applied before the normalisation (cancels) */
+    if (!J->qk_l2norm)
+#endif
+    for (int32_t j = 0; j < dk; ++j) qrow[j] *= scale;
     const double g = widen(J->g, J->f_dtype, gv_off);
     const double b = widen(J->beta, J->f_dtype, gv_off);
     const double vi = widen(J->v, J->qkv_dtype, (t * J->h_v + h) * (int64_t)dv + i);
@@ -309,7 +342,7 @@ int gdn_oracle_prefill(int qkv_dtype, int f_dtype, const void* q, const void* k,
                        const void* v, const void* g, const void* beta,
                        const void* state_in, const int32_t* cu_seqlens,
                        int32_t num_seqs, int64_t total_tokens, int32_t h_k,
-                       int32_t h_v, int32_t d_k, int32_t d_v, double scale,
+                       int32_t h_v, int32_t d_k, int32_t d_v, double scale, int qk_l2norm,
                        double* o_out, double* state_out, int32_t threads) {
   job_t J;
   memset(&J, 0, sizeof J);
@@ -317,6 +350,7 @@ int gdn_oracle_prefill(int qkv_dtype, int f_dtype, const void* q, const void* k,
   J.qkv_dtype = qkv_dtype; J.f_dtype = f_dtype; J.cu = cu_seqlens;
   J.num_seqs = num_seqs; J.total_tokens = total_tokens;
   J.h_k = h_k; J.h_v = h_v; J.d_k = d_k; J.d_v = d_v; J.scale = scale;
+  J.qk_l2norm = qk_l2norm;
   J.o_full = o_out; J.state_full = state_out;
   int rc = check_common(&J);
   if (rc) return rc;
@@ -334,7 +368,8 @@ int gdn_oracle_rows(int qkv_dtype, int f_dtype, const void* q, const void* k,
                     const void* v, const void* g, const void* beta,
                     const void* state_in, const int32_t* cu_seqlens,
                     int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
-                    int32_t d_k, int32_t d_v, double scale, const int64_t* tasks,
+                    int32_t d_k, int32_t d_v, double scale, int qk_l2norm,
+                    const int64_t* tasks,
                     int64_t num_tasks, const int64_t* o_off, double* o_out,
                     double* state_out, int32_t threads) {
   job_t J;
@@ -343,6 +378,7 @@ int gdn_oracle_rows(int qkv_dtype, int f_dtype, const void* q, const void* k,
   J.qkv_dtype = qkv_dtype; J.f_dtype = f_dtype; J.cu = cu_seqlens;
   J.num_seqs = num_seqs; J.total_tokens = total_tokens;
   J.h_k = h_k; J.h_v = h_v; J.d_k = d_k; J.d_v = d_v; J.scale = scale;
+  J.qk_l2norm = qk_l2norm;
   J.tasks = tasks; J.num_tasks = num_tasks; J.o_task = o_out;
   J.state_task = state_out; J.o_task_off = o_off;
   int rc = check_common(&J);

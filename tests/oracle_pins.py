@@ -336,7 +336,35 @@ def pin_rows_match_full(mutant=0):
         assert np.array_equal(sn, st[n, h, i])
 
 
+def pin_qk_l2norm(mutant=0):
+    """In-kernel L2 normalisation of q and k (per token and key head, eps 1e-6
+    inside the square root): (a) the result does not change when any token's q
+    or k is multiplied by a positive number; (b) on unit-norm q and k it equals
+    the plain evaluation up to the eps (relative 1e-6); (c) o is still linear in
+    `scale` (the scale acts after the normalisation)."""
+    lengths = [9, 5]
+    h_k, h_v, d_k, d_v = 1, 2, 6, 4
+    q, k, v, g, beta, s0, cu = _rand_case(17, lengths, h_k, h_v, d_k, d_v)
+    r = _rng(18)
+    cq = np.exp(r.uniform(0, 3, (q.shape[0], h_k, 1)))  # norms >= 1: the eps moves < 1e-6
+    ck = np.exp(r.uniform(0, 3, (k.shape[0], h_k, 1)))
+
+    def run(qq, kk, scale=1.0, norm=True):
+        return oracle.prefill(qq, kk, v, g, beta, cu, h_k, h_v, d_k, d_v, state_in=s0,
+                              scale=scale, threads=4, mutant=mutant, qk_l2norm=norm)
+
+    o_n, st_n = run(q, k)
+    o_s, st_s = run(q * cq, k * ck)
+    _close(o_s, o_n, 1e-5, "o under rescaled q, k")
+    _close(st_s, st_n, 1e-5, "state under rescaled q, k")
+    o_p, st_p = run(q, k, norm=False)  # q, k of _rand_case have unit norm
+    _close(o_n, o_p, 1e-5, "o on unit-norm inputs")
+    _close(st_n, st_p, 1e-5, "state on unit-norm inputs")
+    o_h, _ = run(q * cq, k * ck, scale=0.5)
+    _close(o_h, 0.5 * o_s, TOL, "o linear in scale")
+
+
 ALL_PINS = [pin_brute_force, pin_brute_force_no_state, pin_exact_rational, pin_single_token,
             pin_no_write_no_decay, pin_pure_decay, pin_reset, pin_exact_write, pin_linearity,
             pin_chunked_equals_sequential, pin_row_identity, pin_split_prefill,
-            pin_varlen_packing, pin_rows_match_full]
+            pin_varlen_packing, pin_rows_match_full, pin_qk_l2norm]

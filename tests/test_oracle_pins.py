@@ -16,8 +16,9 @@ def test_pin(pin):
 # Each planted mistake in the oracle (gate not exponentiated, dropped or
 # sign-flipped delta correction, unscaled write, readout with k, readout before
 # the update, wrong head map, gate ignored, gate on the write, transposed state,
-# scale ignored) must make at least one pin fail.
-MUTANTS = list(range(1, 12))
+# scale ignored, q left unnormalised, scale applied before the normalisation)
+# must make at least one pin fail.
+MUTANTS = list(range(1, 14))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
