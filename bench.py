@@ -361,6 +361,36 @@ def main():
     hbm_bytes = prefill_bytes(T, 1, h_k, h_v, d_k, d_v, 2, False)
     roof["hbm_gbs_at_algorithmic_bytes"] = hbm_bytes / (ms_per_step / 1e3) / 1e9
 
+    # the same prefill with the in-kernel q/k L2 normalisation, on raw N(0, 1) q and k
+    dq = inputs.make_prefill(lengths, h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + n0 + 1,
+                             unit_qk=False)
+    xq = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dq.items()}
+    ws_q = torch.empty(max(gdn_prefill_workspace_size(1, T, h_k, h_v, d_k, d_v, torch.bfloat16,
+                                                      "chunked_split"), 16),
+                       dtype=torch.uint8, device=dev)
+
+    def prefill_qk():
+        gdn_prefill(xq["q"], xq["k"], xq["v"], xq["g"], xq["beta"], xq["cu_seqlens"],
+                    state_in=None, state_out=st, o=o, algo=args.algo, workspace=ws_q,
+                    stream=stream, qk_l2norm=True)
+
+    for _ in range(args.warmup):
+        flush()
+        prefill_qk()
+    qk_ms = []
+    for _ in range(args.steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        prefill_qk()
+        b.record(stream)
+        torch.cuda.synchronize()
+        qk_ms.append(a.elapsed_time(b))
+    qk_variant = {"ms_per_step": statistics.median(qk_ms),
+                  "tok_s": T / (statistics.median(qk_ms) / 1e3),
+                  "vs_without": ms_per_step / statistics.median(qk_ms)}
+    del xq, dq, ws_q
+
     # e2e: host buffers in, results out, through the same call
     pin = {k: d[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
     cu_host = d["cu_seqlens"].pin_memory()
@@ -416,6 +446,7 @@ def main():
                                    "exchange)") if world > 1 else "single GPU",
                    "algo": algo_used, "l2": "flushed between timed steps (2x L2 buffer written)"},
         "roofline": roof,
+        "prefill_qk_l2norm": qk_variant,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
         "clocks": clk,
@@ -461,6 +492,27 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
     out["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic("decode_step"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
+
+    # the same step with the in-kernel q/k L2 normalisation
+    def qstep():
+        gdn_decode_step(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"], o=o, stream=stream,
+                        qk_l2norm=True)
+
+    for _ in range(args.warmup):
+        qstep()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        qstep()
+        b.record(stream)
+    torch.cuda.synchronize()
+    qms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    out["decode_b256_qk_l2norm"] = {"us_per_step": qms * 1e3,
+                                    "gbs": nbytes / (qms / 1e3) / 1e9,
+                                    "frac_of_measured_hbm": nbytes / (qms / 1e3) / 1e9 /
+                                    peaks["hbm_gbs"]}
 
     # the same 256 sequences advanced by 4 tokens in one launch (gdn_decode_multi),
     # without and with the per-token state snapshots

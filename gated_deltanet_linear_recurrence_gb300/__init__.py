@@ -58,14 +58,19 @@ def gdn_prefill_workspace_size(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype
                                                       _DTYPES[dtype], _lib.ALGOS[algo]))
 
 
+def _options(qk_l2norm):
+    return _lib.GDN_OPT_QK_L2NORM if qk_l2norm else 0
+
+
 def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=None, scale=1.0,
-                algo="auto", workspace=None, stream=None):
+                algo="auto", workspace=None, stream=None, qk_l2norm=False):
     """Prefill N packed sequences (see gdn_prefill in include/gdn.h).
 
     q, k [T, h_k, d_k]; v [T, h_v, d_v] (fp32 or bf16); g, beta [T, h_v] fp32;
     cu_seqlens [N+1] int32 on the device; state_in [N, h_v, d_v, d_k] fp32 or
     None (zeros).  Returns (o [T, h_v, d_v], state_out [N, h_v, d_v, d_k]).
     ``algo``: "auto", "scan", "chunked", "chunked_fused" or "chunked_split".
+    ``qk_l2norm``: divide q and k by their per-head L2 norm inside the kernels.
     Without ``workspace`` one of the size gdn_prefill_workspace_size() reports
     is allocated (none when that is 0).
     """
@@ -87,14 +92,16 @@ def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=N
         state_out = torch.empty((N, h_v, d_v, d_k), dtype=torch.float32, device=q.device)
     if state_in is not None:
         _require(state_in.dtype == torch.float32 and state_in.is_contiguous(), "state_in fp32")
-    need = lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt, _lib.ALGOS[algo])
+    # with the normalisation option the chunked form is the two-kernel one
+    ws_algo = "chunked_split" if (qk_l2norm and algo in ("auto", "chunked")) else algo
+    need = lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt, _lib.ALGOS[ws_algo])
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
-                         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), N, T, h_k, h_v, d_k, d_v,
-                         dt, float(scale), _lib.ALGOS[algo], _ptr(workspace), ws_bytes,
-                         _stream(stream))
+    st = lib.gdn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                            _ptr(state_out), _ptr(o), _ptr(cu_seqlens), N, T, h_k, h_v, d_k, d_v,
+                            dt, float(scale), _lib.ALGOS[algo], _ptr(workspace), ws_bytes,
+                            _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_prefill")
     return o, state_out
 
@@ -105,7 +112,7 @@ def gdn_prefill_streamed_workspace_size(piece_tokens, h_k, h_v, d_k, d_v, dtype=
 
 
 def gdn_prefill_streamed(q, k, v, g, beta, piece_tokens, state_in=None, state_out=None, o=None,
-                         scale=1.0, workspace=None, stream=None):
+                         scale=1.0, workspace=None, stream=None, qk_l2norm=False):
     """One sequence (q, k [T, h_k, d_k]; v [T, h_v, d_v]; g, beta [T, h_v]) prefilled
     as pieces of ``piece_tokens`` tokens (a multiple of 64) with the state carried
     between them (gdn_prefill_streamed in include/gdn.h).  Returns (o, state_out
@@ -131,7 +138,7 @@ def gdn_prefill_streamed(q, k, v, g, beta, piece_tokens, state_in=None, state_ou
     st = lib.gdn_prefill_streamed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
                                   _ptr(state_out), _ptr(o), T, h_k, h_v, d_k, d_v, dt,
                                   float(scale), int(piece_tokens), _ptr(workspace), ws_bytes,
-                                  _stream(stream))
+                                  _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_prefill_streamed")
     return o, state_out
 
@@ -162,7 +169,7 @@ def gdn_prefill_noalloc(q, k, v, g, beta, cu_seqlens, state_out, o, state_in=Non
     return o, state_out
 
 
-def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None):
+def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None, qk_l2norm=False):
     """One token per sequence, state [B, h_v, d_v, d_k] fp32 updated in place.
 
     q, k [B, h_k, d_k]; v [B, h_v, d_v]; g, beta [B, h_v] fp32.  Returns o [B, h_v, d_v].
@@ -179,13 +186,15 @@ def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None):
     dt = _dtype_code(q)
     if o is None:
         o = torch.empty((B, h_v, d_v), dtype=q.dtype, device=q.device)
-    st = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                             _ptr(o), B, h_k, h_v, d_k, d_v, dt, float(scale), _stream(stream))
+    st = lib.gdn_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                _ptr(o), B, h_k, h_v, d_k, d_v, dt, float(scale),
+                                _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_decode_step")
     return o
 
 
-def gdn_decode_multi(q, k, v, g, beta, state, o=None, snapshots=False, scale=1.0, stream=None):
+def gdn_decode_multi(q, k, v, g, beta, state, o=None, snapshots=False, scale=1.0, stream=None,
+                     qk_l2norm=False):
     """n tokens for each of B sequences in one launch (gdn_decode_multi in
     include/gdn.h): q, k [B, n, h_k, d_k]; v [B, n, h_v, d_v]; g, beta [B, n, h_v]
     fp32; state [B, h_v, d_v, d_k] fp32 updated in place to the state after the
@@ -214,7 +223,7 @@ def gdn_decode_multi(q, k, v, g, beta, state, o=None, snapshots=False, scale=1.0
                  snap.is_contiguous(), "snapshots must be [B, n, h_v, d_v, d_k] fp32")
     st = lib.gdn_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                               _ptr(o), _ptr(snap), B, n, h_k, h_v, d_k, d_v, dt, float(scale),
-                              _stream(stream))
+                              _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_decode_multi")
     return o if snap is None else (o, snap)
 

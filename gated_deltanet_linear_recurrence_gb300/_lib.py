@@ -17,6 +17,7 @@ STATUS_NAMES = {
     9: "GDN_ERR_CUDA",
 }
 GDN_F32, GDN_BF16 = 0, 1
+GDN_OPT_QK_L2NORM = 1
 ALGOS = {"auto": 0, "scan": 1, "chunked": 2, "chunked_fused": 3, "chunked_split": 4}
 
 # Exported symbols, with ctypes signatures: (restype, argtypes)
@@ -26,11 +27,16 @@ SIGNATURES = {
     "gdn_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32,
                                    _i32, _i32, _i32, ctypes.c_int, _f32, ctypes.c_int, _vp, _sz,
                                    _vp]),
+    "gdn_prefill_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64,
+                                      _i32, _i32, _i32, _i32, ctypes.c_int, _f32, ctypes.c_int,
+                                      _vp, _sz, ctypes.c_uint32, _vp]),
+    "gdn_decode_step_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                          _i32, _i32, ctypes.c_int, _f32, ctypes.c_uint32, _vp]),
     "gdn_prefill_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32, ctypes.c_int,
                                          ctypes.c_int]),
     "gdn_prefill_streamed": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32,
                                             _i32, _i32, _i32, ctypes.c_int, _f32, _i64, _vp, _sz,
-                                            _vp]),
+                                            ctypes.c_uint32, _vp]),
     "gdn_prefill_streamed_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32, ctypes.c_int]),
     "gdn_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                            _i64, _i32, _i32, _i32, _i32, ctypes.c_int, _f32,
@@ -38,7 +44,8 @@ SIGNATURES = {
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                        _i32, ctypes.c_int, _f32, _vp]),
     "gdn_decode_multi": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
-                                        _i32, _i32, _i32, ctypes.c_int, _f32, _vp]),
+                                        _i32, _i32, _i32, ctypes.c_int, _f32, ctypes.c_uint32,
+                                        _vp]),
     "gdn_stream_status": (ctypes.c_int, [_vp]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_prefill_crossover_tokens": (_i32, [_i32, _i32, _i32, _i32, ctypes.c_int]),

@@ -79,6 +79,7 @@ struct SplitParams {
   int32_t h_k, h_v, d_v;
   float scale;
   int32_t min_len;
+  int qk_norm;          // q and k divided by their L2 norm (+1e-6 under the root)
   int32_t* chunk_base;  // [N+1] in the workspace header
   uint8_t* packages;    // items x kPkgBytes
   int64_t max_items;
@@ -157,14 +158,16 @@ constexpr uint32_t kBarAll = 1, kBarGateP = 2;
 //   [0, 32K)     per d_k half kb: [Q 8K][K 8K] (TMA); after G: Q1 holds the
 //                solve scratch, then T diag(b Gamma); after W: K holds V (TMA)
 //   [32K, 49K)   A, then T: fp32 [64][kLdM]; then T diag(b) (bf16) at its start
-//   gates        Gamma[64], decay[64], Gamma_n, then gamma[64], beta[64]
+//   gates        Gamma[64], decay[64], Gamma_n, then gamma[64], beta[64], and the
+//                reciprocal L2 norms of the chunk's k rows and q rows (1 without
+//                the normalisation option)
 constexpr uint32_t PP_KQ = 0;
 constexpr uint32_t PP_Q1 = 16384;                  // solve scratch, then T diag(b Gamma)
 constexpr uint32_t PP_V = 8192;                    // V halves over K0 and K1 (stride 16K)
 constexpr uint32_t PP_MF = 32768;
 constexpr uint32_t PP_TA = PP_MF;                  // T diag(b), once T is in registers
 constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;
-constexpr uint32_t PP_MISC = PP_GATE + 5 * 64 * 4;
+constexpr uint32_t PP_MISC = PP_GATE + 7 * 64 * 4;
 constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
 static_assert(4 * (kPrepSmem + 1024) <= 233472, "four prepare CTAs per SM");
 constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W, then U~ (0-127)
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   float* YF = reinterpret_cast<float*>(smem + PP_Q1);
   float* gsm = reinterpret_cast<float*>(smem + PP_GATE);
   float *Gam = gsm, *dec = gsm + 64, *gam = gsm + 192, *bet = gsm + 256;
+  float *rk = gsm + 320, *rq = gsm + 384;
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);  // Q, K
   uint64_t* bar_mma = bar_tma + 1;
   uint64_t* bar_v = bar_tma + 2;                                     // V (needed only for U~)
@@ -252,6 +256,30 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
       tc::mma_commit(bar_mma);
     }
+    {  // 1 / |row| of K (threads 0-63) and Q (64-127) with the normalisation option, else 1
+      float r = 1.f;
+      if (p.qk_norm) {
+        const int t = pt & 63;
+        const uint8_t* base = smem + PP_KQ + (pt < 64 ? 8192 : 0);
+        float ss = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(
+                base + kb * 16384 + tc::swizzle<3>(t * 128 + c8 * 16));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+              ss = fmaf(lo, lo, ss);
+              ss = fmaf(hi, hi, ss);
+            }
+          }
+        r = rsqrtf(ss + 1e-6f);
+      }
+      (pt < 64 ? rk : rq)[pt & 63] = r;
+    }
     if (pt < 64) {  // gates: inclusive scan of g over the chunk
       float x = gr;
 #pragma unroll
@@ -267,20 +295,23 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       bet[pt] = br;
       tc::named_sync(kBarGateP, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
-      float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
-      gout[pt] = Gam[pt];
-      gout[64 + pt] = dec[pt];
-      if (pt == 0) gout[128] = Gam[kC - 1];
     }
     ok = tc::mbar_wait(bar_mma, 0);
     tc::fence_after_sync();
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (pt < 64) {  // the chain's per-row factors: Gamma_r / |q_r| for the output, decay_r / |k_r|
+      float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
+      gout[pt] = Gam[pt] * rq[pt];
+      gout[64 + pt] = dec[pt] * rk[pt];
+      if (pt == 0) gout[128] = Gam[kC - 1];
+    }
   }
   if (ok) {
     // masks, one G row per thread (TMEM lane pt): P rows (warps 0, 1) to the
     // package, A rows (warps 2, 3) to MF; 32 columns at a time
     const int r = 32 * (pw & 1) + lane;
     const float g_r = gam[r], b_r = bet[r];
+    const float n_r = pw < 2 ? rq[r] : rk[r];  // q_r for P rows, k_r for A rows
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
       const int i0 = 32 * half;
@@ -290,11 +321,12 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-          const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+          const float4 ki = *reinterpret_cast<const float4*>(rk + i0 + 4 * e4);
+          const float gv[4] = {gi.x, gi.y, gi.z, gi.w}, kv[4] = {ki.x, ki.y, ki.z, ki.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int e = 4 * e4 + q, i = i0 + e;
-            a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] : 0.f;
+            a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] * (n_r * kv[q]) : 0.f;
           }
         }
 #pragma unroll
@@ -304,12 +336,14 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-          const float gv[4] = {gi.x, gi.y, gi.z, gi.w};
+          const float4 ki = *reinterpret_cast<const float4*>(rk + i0 + 4 * e4);
+          const float gv[4] = {gi.x, gi.y, gi.z, gi.w}, kv[4] = {ki.x, ki.y, ki.z, ki.w};
           float o4[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int i = i0 + 4 * e4 + q;
-            o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] : 0.f;
+            o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] * (n_r * kv[q])
+                            : 0.f;
           }
           *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
               make_float4(o4[0], o4[1], o4[2], o4[3]);
@@ -338,7 +372,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           xa[e] = t[8 * c8 + e] * bet[ii + e];
-          xb[e] = xa[e] * Gam[ii + e];
+          xb[e] = xa[e] * Gam[ii + e] * rk[ii + e];  // W = T diag(b Gamma / |k|) K
         }
         st_chunk<3>(smem + PP_TA, rr * 128 + (4 * q + c8) * 16, xa);
         st_chunk<3>(smem + PP_Q1, rr * 128 + (4 * q + c8) * 16, xb);
@@ -787,6 +821,7 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   p.d_v = a.d_v;
   p.scale = a.scale;
   p.min_len = a.min_chunk_len;
+  p.qk_norm = a.qk_norm;
   p.chunk_base = static_cast<int32_t*>(workspace);
   p.packages = static_cast<uint8_t*>(workspace) + split_header_bytes(a.num_seqs);
   p.max_items = (int64_t)split_max_items(a.num_seqs, a.total_tokens, a.h_v);

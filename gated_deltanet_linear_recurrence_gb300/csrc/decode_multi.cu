@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kMultiWarps * 32)
                         const float* __restrict__ g, const float* __restrict__ beta,
                         float* __restrict__ state, T* __restrict__ o, float* __restrict__ snap,
                         int32_t n_tok, int32_t h_k, int32_t h_v, int32_t d_v,
-                        int32_t blocks_per_head, float scale) {
+                        int32_t blocks_per_head, float scale, int qk_norm) {
   constexpr int L = DK / 4;
   using LY = RowLayout<DK, L, R>;
   constexpr int M = LY::M;
@@ -66,6 +66,13 @@ __global__ void __launch_bounds__(kMultiWarps * 32)
     for (int m = 0; m < M; ++m) {
       k4[m] = load4(kp + 4 * L * m);
       q4[m] = load4(qp + 4 * L * m);
+    }
+    if (qk_norm) {
+      l2_normalize<L, M>(k4);
+      l2_normalize<L, M>(q4);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
       q4[m].x *= scale;
       q4[m].y *= scale;
       q4[m].z *= scale;
@@ -108,7 +115,7 @@ cudaError_t launch_t(const DecodeMultiArgs& a, cudaStream_t stream) {
   decode_multi_kernel<DK, R, T><<<grid, kMultiWarps * 32, 0, stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
       a.beta, a.state, static_cast<T*>(a.o), a.snapshots, a.n_tokens, a.h_k, a.h_v, a.d_v,
-      blocks_per_head, a.scale);
+      blocks_per_head, a.scale, a.qk_norm);
   return cudaGetLastError();
 }
 

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const float* __restrict__ g, const float* __restrict__ beta,
                        float* __restrict__ state, T* __restrict__ o, int32_t h_k, int32_t h_v,
-                       int32_t d_v, int32_t blocks_per_head, float scale) {
+                       int32_t d_v, int32_t blocks_per_head, float scale, int qk_norm) {
   constexpr int L = DK / 4;  // one float4 per lane per row
   using LY = RowLayout<DK, L, R>;
   constexpr int M = LY::M;
@@ -62,6 +62,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   for (int m = 0; m < M; ++m) {
     k4[m] = load4(kp + 4 * L * m);
     q4[m] = load4(qp + 4 * L * m);
+  }
+  if (qk_norm) {
+    l2_normalize<L, M>(k4);
+    l2_normalize<L, M>(q4);
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
     q4[m].x *= scale;
     q4[m].y *= scale;
     q4[m].z *= scale;
@@ -99,7 +106,8 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   dim3 grid((unsigned)gx, (unsigned)a.h_v);
   decode_step_kernel<DK, R, T><<<grid, kDecodeWarps * 32, 0, stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
-      a.beta, a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale);
+      a.beta, a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale,
+      a.qk_norm);
   return cudaGetLastError();
 }
 

@@ -109,7 +109,19 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
                        int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                        float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
                        gdn_stream_t stream) {
+  return gdn_prefill_ex(q, k, v, g, beta, state_in, state_out, o, cu_seqlens, num_seqs,
+                        total_tokens, h_k, h_v, d_k, d_v, dtype, scale, algo, workspace,
+                        workspace_bytes, 0u, stream);
+}
+
+gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const float* state_in, float* state_out, void* o,
+                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                          float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                          uint32_t options, gdn_stream_t stream) {
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
   if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED &&
       algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT)
     return GDN_ERR_INVALID_ARG;
@@ -130,6 +142,10 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     const char* b = reinterpret_cast<const char*>(state_out);
     if (a < b + state_bytes && b < a + state_bytes) return GDN_ERR_INVALID_ARG;
   }
+  const bool qk_norm = (options & GDN_OPT_QK_L2NORM) != 0;
+  // With the normalisation option the chunked evaluation is the two-kernel one
+  // (the fused kernel does not implement the option).
+  if (qk_norm && algo == GDN_ALGO_CHUNKED_FUSED) return GDN_ERR_INVALID_ARG;
   const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
   const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
                           algo == GDN_ALGO_CHUNKED_SPLIT;
@@ -142,6 +158,7 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
   a.num_seqs = num_seqs; a.total_tokens = total_tokens;
   a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
   a.dtype = dtype; a.scale = scale;
+  a.qk_norm = qk_norm ? 1 : 0;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
 
   // Which kernels run: scan for sequences shorter than min_chunk_len, chunked
@@ -171,7 +188,13 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
     }
     if (workspace && !aligned16(workspace)) return GDN_ERR_MISALIGNED;
     split = workspace && workspace_bytes >= need &&
-            (algo == GDN_ALGO_CHUNKED_SPLIT || split_preferred(num_seqs, total_tokens));
+            (algo == GDN_ALGO_CHUNKED_SPLIT || qk_norm || split_preferred(num_seqs, total_tokens));
+    if (qk_norm && !split) {  // no room for the two kernels: the token scan takes everything
+      if (algo == GDN_ALGO_CHUNKED) return GDN_ERR_WORKSPACE_TOO_SMALL;
+      run_chunk = false;
+      run_scan = true;
+      a.min_chunk_len = INT32_MAX;
+    }
   }
   st = error_word(&a.err);
   if (st != GDN_OK) return st;
@@ -189,7 +212,16 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            const float* beta, float* state, void* o, int32_t batch, int32_t h_k,
                            int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
                            gdn_stream_t stream) {
+  return gdn_decode_step_ex(q, k, v, g, beta, state, o, batch, h_k, h_v, d_k, d_v, dtype, scale,
+                            0u, stream);
+}
+
+gdn_status gdn_decode_step_ex(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* state, void* o, int32_t batch,
+                              int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                              float scale, uint32_t options, gdn_stream_t stream) {
   if (batch < 0) return GDN_ERR_INVALID_ARG;
+  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
   gdn_status st = check_heads(h_k, h_v, d_k, d_v);
   if (st != GDN_OK) return st;
@@ -202,6 +234,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.o = o;
   a.batch = batch; a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
   a.dtype = dtype; a.scale = scale;
+  a.qk_norm = (options & GDN_OPT_QK_L2NORM) ? 1 : 0;
   if (gdn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GDN_ERR_CUDA;
   return GDN_OK;
@@ -211,8 +244,9 @@ gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const f
                             const float* beta, float* state, void* o, float* snapshots,
                             int32_t batch, int32_t n_tokens, int32_t h_k, int32_t h_v,
                             int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
-                            gdn_stream_t stream) {
+                            uint32_t options, gdn_stream_t stream) {
   if (batch < 0 || n_tokens < 1 || n_tokens > 1024) return GDN_ERR_INVALID_ARG;
+  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
   gdn_status st = check_heads(h_k, h_v, d_k, d_v);
   if (st != GDN_OK) return st;
@@ -232,6 +266,7 @@ gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const f
   a.snapshots = snapshots;
   a.batch = batch; a.n_tokens = n_tokens; a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
   a.dtype = dtype; a.scale = scale;
+  a.qk_norm = (options & GDN_OPT_QK_L2NORM) ? 1 : 0;
   if (gdn::launch_decode_multi(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GDN_ERR_CUDA;
   return GDN_OK;

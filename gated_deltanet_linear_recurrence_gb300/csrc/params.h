@@ -23,6 +23,7 @@ struct DecodeArgs {
   int32_t batch, h_k, h_v, d_k, d_v;
   int dtype;
   float scale;
+  int qk_norm;  // divide q and k by their L2 norm (+1e-6 under the root) first
 };
 
 // Several tokens per sequence: q, k [B][n][h_k][d_k], v, o [B][n][h_v][d_v],
@@ -40,6 +41,7 @@ struct DecodeMultiArgs {
   int32_t batch, n_tokens, h_k, h_v, d_k, d_v;
   int dtype;
   float scale;
+  int qk_norm;
 };
 
 struct PrefillArgs {
@@ -57,6 +59,7 @@ struct PrefillArgs {
   int32_t h_k, h_v, d_k, d_v;
   int dtype;
   float scale;
+  int qk_norm;  // divide q and k by their L2 norm (+1e-6 under the root) first
   // Per-sequence split between the two evaluations: a sequence of length L
   // is handled by the scan when L < min_chunk_len and by the chunked kernel
   // otherwise.  (0 = chunked takes every sequence; INT32_MAX = scan takes all.)

@@ -91,6 +91,25 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
+// x <- x / sqrt(|x|^2 + 1e-6) for a vector of d_k values spread over the L
+// lanes of a lane group (M float4 chunks per lane): the optional per-head L2
+// normalisation of q and k.
+template <int L, int M>
+__device__ __forceinline__ void l2_normalize(float4 (&x)[M]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < M; ++m) ss = dot4(x[m], x[m], ss);
+  ss = group_sum<L>(ss);
+  const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    x[m].x *= r;
+    x[m].y *= r;
+    x[m].z *= r;
+    x[m].w *= r;
+  }
+}
+
 template <int DK, int L, int R>
 struct RowLayout {
   static constexpr int M = DK / (4 * L);  // float4 chunks per lane per row

@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kScanWarps * 32)
                         const float* __restrict__ beta, const float* state_in, float* state_out,
                         T* __restrict__ o, const int32_t* __restrict__ cu, int32_t num_seqs,
                         int64_t total_tokens, int32_t h_k, int32_t h_v, int32_t d_v,
-                        int32_t blocks_per_head, float scale, int32_t max_len, int* err) {
+                        int32_t blocks_per_head, float scale, int32_t max_len, int qk_norm,
+                        int* err) {
   using LY = RowLayout<DK, L, R>;
   constexpr int M = LY::M;
   const int lane = threadIdx.x & 31;
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(kScanWarps * 32)
     if (t + 1 < t1)
       load_token<DK, L, M, T>(nxt, q, k, v, g, beta, t + 1, h_k, h_v, d_v, hk, h, lam,
                               row_mine);
+    if (qk_norm) {
+      l2_normalize<L, M>(cur.k4);
+      l2_normalize<L, M>(cur.q4);
+    }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       cur.q4[m].x *= scale;
@@ -141,7 +146,8 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t stream) {
   scan_prefill_kernel<DK, L, R, T><<<grid, kScanWarps * 32, 0, stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
       a.beta, a.state_in, a.state_out, static_cast<T*>(a.o), a.cu_seqlens, a.num_seqs,
-      a.total_tokens, a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale, a.min_chunk_len, a.err);
+      a.total_tokens, a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale, a.min_chunk_len, a.qk_norm,
+      a.err);
   return cudaGetLastError();
 }
 

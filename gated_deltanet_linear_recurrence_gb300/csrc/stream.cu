@@ -72,7 +72,7 @@ gdn_status gdn_prefill_streamed(const void* q, const void* k, const void* v, con
                                 void* o, int64_t total_tokens, int32_t h_k, int32_t h_v,
                                 int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
                                 int64_t piece_tokens, void* workspace, size_t workspace_bytes,
-                                gdn_stream_t stream) {
+                                uint32_t options, gdn_stream_t stream) {
   if (total_tokens < 0 || piece_tokens <= 0 || piece_tokens % kPieceQuantum ||
       piece_tokens > INT32_MAX)
     return GDN_ERR_INVALID_ARG;
@@ -105,13 +105,13 @@ gdn_status gdn_prefill_streamed(const void* q, const void* k, const void* v, con
     const int64_t t0 = i * piece_tokens;
     const int64_t len = i == n_pieces - 1 ? last : piece_tokens;
     const int32_t* cu_i = i == n_pieces - 1 ? cu + 4 : cu;
-    const gdn_status st = gdn_prefill(
+    const gdn_status st = gdn_prefill_ex(
         q ? static_cast<const char*>(q) + t0 * qk_row : nullptr,
         k ? static_cast<const char*>(k) + t0 * qk_row : nullptr,
         v ? static_cast<const char*>(v) + t0 * vo_row : nullptr, g ? g + t0 * h_v : nullptr,
         beta ? beta + t0 * h_v : nullptr, i == 0 ? state_in : state_out, state_out,
         o ? static_cast<char*>(o) + t0 * vo_row : nullptr, cu_i, 1, len, h_k, h_v, d_k, d_v,
-        dtype, scale, algo, piece_ws, workspace_bytes - kHeadBytes, stream);
+        dtype, scale, algo, piece_ws, workspace_bytes - kHeadBytes, options, stream);
     if (st != GDN_OK) return st;
   }
   return GDN_OK;

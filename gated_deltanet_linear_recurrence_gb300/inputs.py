@@ -35,12 +35,12 @@ def _unit_rows(x):
     return x / x.norm(dim=-1, keepdim=True)
 
 
-def _draw_qk(gen, tokens, heads, dim, dtype):
+def _draw_qk(gen, tokens, heads, dim, dtype, unit=True):
     out = torch.empty((tokens, heads, dim), dtype=dtype)
     for t0 in range(0, tokens, _BLOCK_TOKENS):
         t1 = min(tokens, t0 + _BLOCK_TOKENS)
         blk = torch.randn((t1 - t0, heads, dim), generator=gen, dtype=torch.float64)
-        out[t0:t1] = _unit_rows(blk).to(dtype)
+        out[t0:t1] = (_unit_rows(blk) if unit else blk).to(dtype)
     return out
 
 
@@ -70,19 +70,21 @@ def cu_from_lengths(lengths):
     return torch.tensor(cu, dtype=torch.int32)
 
 
-def make_prefill(lengths, h_k, h_v, d_k, d_v, dtype="bf16", seed=0, state_std=0.0):
+def make_prefill(lengths, h_k, h_v, d_k, d_v, dtype="bf16", seed=0, state_std=0.0,
+                 unit_qk=True):
     """Packed varlen prefill inputs on the host.
 
     Returns a dict with q, k [T, h_k, d_k]; v [T, h_v, d_v] (dtype); g, beta
     [T, h_v] fp32; state_in [N, h_v, d_v, d_k] fp32 or None (zeros);
-    cu_seqlens [N+1] int32.
+    cu_seqlens [N+1] int32.  ``unit_qk=False`` leaves q and k as drawn, N(0, 1)
+    (inputs for the in-kernel normalisation option).
     """
     dt = DTYPES[dtype]
     cu = cu_from_lengths(lengths)
     T = int(cu[-1])
     gen = _gen(seed)
-    q = _draw_qk(gen, T, h_k, d_k, dt)
-    k = _draw_qk(gen, T, h_k, d_k, dt)
+    q = _draw_qk(gen, T, h_k, d_k, dt, unit_qk)
+    k = _draw_qk(gen, T, h_k, d_k, dt, unit_qk)
     v = _draw_normal(gen, (T, h_v, d_v), dt)
     g, beta = _draw_gates(gen, T, h_v)
     state = None

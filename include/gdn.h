@@ -71,6 +71,19 @@ typedef enum {
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype; /* dtype of q, k, v and o */
 
+/*
+ * Options of the *_ex entry points, gdn_decode_multi and gdn_prefill_streamed
+ * (bitwise OR; 0 = the plain recurrence).
+ *
+ * GDN_OPT_QK_L2NORM: divide q and k of every (token, key head) by
+ * sqrt(sum of squares + 1e-6) before the recurrence (q is then multiplied by
+ * `scale`).  Page "Optimizing on-device inference for Apple Silicon", section
+ * "Reduce intermediate and state traffic": the decode path fuses the recurrent
+ * update with its normalization; per-head L2 normalisation of q and k is the
+ * reading taken here, done inside the kernels instead of as a separate pass.
+ */
+#define GDN_OPT_QK_L2NORM 1u
+
 typedef enum {
   GDN_ALGO_AUTO = 0,          /* per sequence: scan below the measured crossover length, else chunked */
   GDN_ALGO_SCAN = 1,          /* token scan, state rows resident in registers (fp32 and bf16) */
@@ -113,6 +126,20 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float*
                        float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
                        gdn_stream_t stream);
 
+/* gdn_prefill with `options` (see GDN_OPT_QK_L2NORM); other bits return
+ * GDN_ERR_INVALID_ARG.  gdn_prefill is gdn_prefill_ex with options = 0.
+ * With GDN_OPT_QK_L2NORM the chunked evaluation is the two-kernel form only:
+ * GDN_ALGO_CHUNKED_FUSED returns GDN_ERR_INVALID_ARG, GDN_ALGO_CHUNKED needs a
+ * workspace of gdn_prefill_workspace_size(..., GDN_ALGO_CHUNKED_SPLIT) bytes
+ * (else GDN_ERR_WORKSPACE_TOO_SMALL), and GDN_ALGO_AUTO without such a
+ * workspace runs the token scan for every sequence. */
+gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const float* state_in, float* state_out, void* o,
+                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                          float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                          uint32_t options, gdn_stream_t stream);
+
 /* Bytes of workspace for the fastest gdn_prefill path with these arguments
  * (0 when that path uses none); for GDN_ALGO_CHUNKED_SPLIT, the bytes it
  * needs.  An upper bound computed from the host arguments: the 1 KB-rounded
@@ -138,14 +165,15 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  * sequence.  workspace: required, 16-byte aligned, at least
  * gdn_prefill_streamed_workspace_size(piece_tokens, ...) bytes, which does not
  * depend on total_tokens.  Errors: GDN_ERR_INVALID_ARG for a bad piece size,
- * GDN_ERR_WORKSPACE_TOO_SMALL, and those of gdn_prefill.
+ * GDN_ERR_WORKSPACE_TOO_SMALL, and those of gdn_prefill.  `options` as for
+ * gdn_prefill_ex.
  */
 gdn_status gdn_prefill_streamed(const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* state_in, float* state_out,
                                 void* o, int64_t total_tokens, int32_t h_k, int32_t h_v,
                                 int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
                                 int64_t piece_tokens, void* workspace, size_t workspace_bytes,
-                                gdn_stream_t stream);
+                                uint32_t options, gdn_stream_t stream);
 
 /* Workspace bytes for gdn_prefill_streamed with pieces of piece_tokens tokens
  * (0 for an invalid piece size or head shape). */
@@ -200,6 +228,12 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
                            gdn_stream_t stream);
 
+/* gdn_decode_step with `options` (see GDN_OPT_QK_L2NORM). */
+gdn_status gdn_decode_step_ex(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* state, void* o, int32_t batch,
+                              int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
+                              float scale, uint32_t options, gdn_stream_t stream);
+
 /*
  * gdn_decode_multi — n_tokens (1 .. 1024) consecutive tokens for each of
  * `batch` sequences in one launch: the state is read once, carried through the
@@ -215,13 +249,13 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
  * fp32, updated in place to the state after the last token; snapshots NULL or
  * [batch][n_tokens][h_v][d_v][d_k] fp32 receiving the state after each token
  * (must not overlap the state).  Same head mapping and scale as
- * gdn_decode_step.
+ * gdn_decode_step; `options` as for gdn_decode_step_ex.
  */
 gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, float* state, void* o, float* snapshots,
                             int32_t batch, int32_t n_tokens, int32_t h_k, int32_t h_v,
                             int32_t d_k, int32_t d_v, gdn_dtype dtype, float scale,
-                            gdn_stream_t stream);
+                            uint32_t options, gdn_stream_t stream);
 
 /*
  * gdn_stream_status — synchronise `stream`, then report (and clear) the

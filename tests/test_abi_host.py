@@ -52,6 +52,18 @@ def prefill(lib, **kw):
                            a["ws_bytes"], a["stream"])
 
 
+def test_options_host_errors(lib):
+    """Unknown option bits are refused before anything is launched."""
+    assert lib.gdn_prefill_ex(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 64, 1, 1,
+                              16, 16, 1, 1.0, 1, None, 0, 4, None) == 2
+    assert lib.gdn_prefill_ex(None, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 64, 1, 1,
+                              16, 16, 1, 1.0, 1, None, 0, 1, None) == 1
+    assert lib.gdn_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 16, 16, 1,
+                                  1.0, 8, None) == 2
+    assert lib.gdn_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 1, 16, 16, 1,
+                                  1.0, 1, None) == 1
+
+
 def test_prefill_host_errors(lib):
     assert prefill(lib, q=None) == 1                     # NULL
     assert prefill(lib, cu=None) == 1
@@ -125,13 +137,14 @@ def test_workspace_and_crossover_queries(lib):
 def test_streamed_host_errors(lib):
     """gdn_prefill_streamed refuses bad arguments before launching anything."""
     def call(t=4096, piece=1024, h_k=16, h_v=32, d_k=128, d_v=128, dtype=1, ws=FAKE,
-             ws_bytes=1 << 40, **ptr):
+             ws_bytes=1 << 40, opts=0, **ptr):
         p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state_in=None, state_out=FAKE, o=FAKE)
         p.update(ptr)
         return lib.gdn_prefill_streamed(p["q"], p["k"], p["v"], p["g"], p["beta"], p["state_in"],
                                         p["state_out"], p["o"], t, h_k, h_v, d_k, d_v, dtype, 1.0,
-                                        piece, ws, ws_bytes, None)
+                                        piece, ws, ws_bytes, opts, None)
     assert call(piece=1000) == 2                         # not whole chunks
+    assert call(opts=6, ws_bytes=4096) in (2, 7)          # an unknown option bit or the size
     assert call(piece=0) == 2
     assert call(t=-1) == 2
     assert call(d_k=48) == 3
@@ -153,11 +166,11 @@ def test_streamed_host_errors(lib):
 
 
 def test_decode_multi_host_errors(lib):
-    def call(b=2, n=3, h_k=1, h_v=1, d_k=16, d_v=16, dtype=1, snap=None, **ptr):
+    def call(b=2, n=3, h_k=1, h_v=1, d_k=16, d_v=16, dtype=1, snap=None, opts=0, **ptr):
         p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE)
         p.update(ptr)
         return lib.gdn_decode_multi(p["q"], p["k"], p["v"], p["g"], p["beta"], p["state"], p["o"],
-                                    snap, b, n, h_k, h_v, d_k, d_v, dtype, 1.0, None)
+                                    snap, b, n, h_k, h_v, d_k, d_v, dtype, 1.0, opts, None)
     assert call(n=0) == 2
     assert call(n=2000) == 2
     assert call(b=-1) == 2
@@ -166,4 +179,5 @@ def test_decode_multi_host_errors(lib):
     assert call(state=None) == 1
     assert call(o=FAKE + 2) == 5
     assert call(snap=FAKE + 16) == 2                     # snapshots overlap the state
+    assert call(opts=2) == 2                             # unknown option bit
     assert call(b=0) == 0
