@@ -40,14 +40,14 @@ FP32_LANES_PER_SM = 128
 # the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "93d024016f3513fb",
-                    "bytes": 5_120 + (68_248_320 + 31_823_104) + (119_582_464 + 15_531_264),
+                    "sha256_16": "0fe1f9896bdaa1ee",
+                    "bytes": 5_376 + (68_257_024 + 28_667_392) + (119_578_112 + 12_312_832),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh"],
-                    "sha256_16": "b48aed3378955542", "bytes": 541_181_952 + 479_234_560,
+                    "sha256_16": "5bd4e2fd057ca7a3", "bytes": 541_150_720 + 479_120_896,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
