@@ -135,3 +135,27 @@ WORKLOADS = {
                              h_v=32, d_k=128, d_v=128, dtype="bf16", state_std=0.0,
                              seed=SEED_BASE + 5),
 }
+
+
+def make_attention(batch, h_q, h_kv, head_dim, capacity, lengths, dtype="bf16", seed=0,
+                   poison_tail=True):
+    """Decode-attention inputs on the host: q [B, h_q, D]; k_cache, v_cache
+    [B, h_kv, capacity, D]; cache_len [B] int32; all N(0, 1) in `dtype`.
+    ``poison_tail`` fills the cache slots past each sequence's length with NaN
+    (they must never reach a result).  Drawn in blocks of cache rows."""
+    dt = DTYPES[dtype]
+    gen = _gen(seed)
+    q = _draw_normal(gen, (batch, h_q, head_dim), dt)
+    k = torch.empty((batch, h_kv, capacity, head_dim), dtype=dt)
+    v = torch.empty((batch, h_kv, capacity, head_dim), dtype=dt)
+    for b in range(batch):
+        for j in range(h_kv):
+            k[b, j] = _draw_normal(gen, (capacity, head_dim), dt)
+            v[b, j] = _draw_normal(gen, (capacity, head_dim), dt)
+    lens = torch.tensor([int(x) for x in lengths], dtype=torch.int32)
+    if poison_tail:
+        for b in range(batch):
+            k[b, :, int(lens[b]):] = float("nan")
+            v[b, :, int(lens[b]):] = float("nan")
+    return dict(q=q, k_cache=k, v_cache=v, cache_len=lens, h_q=h_q, h_kv=h_kv,
+                head_dim=head_dim, capacity=capacity, dtype=dtype)
