@@ -13,7 +13,8 @@ from . import _lib
 from ._lib import GdnError, STATUS_NAMES
 
 __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
-           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi",
+           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi", "gdn_attn_decode",
+           "gdn_attn_decode_workspace_size",
            "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
@@ -226,6 +227,49 @@ def gdn_decode_multi(q, k, v, g, beta, state, o=None, snapshots=False, scale=1.0
                               _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_decode_multi")
     return o if snap is None else (o, snap)
+
+
+def gdn_attn_decode_workspace_size(batch, h_q, h_kv, head_dim, capacity, layout="auto",
+                                   block_keys=0):
+    return int(_lib.load().gdn_attn_decode_workspace_size(batch, h_q, h_kv, head_dim, capacity,
+                                                          _lib.ATTN_LAYOUTS[layout],
+                                                          int(block_keys)))
+
+
+def gdn_attn_decode(q, k_cache, v_cache, cache_len, scale=None, o=None, layout="auto",
+                    block_keys=0, workspace=None, stream=None):
+    """Grouped-query decode attention (gdn_attn_decode in include/gdn.h): q
+    [B, h_q, D]; k_cache, v_cache [B, h_kv, capacity, D]; cache_len [B] int32 on
+    the device; all bf16, D = 256, h_q / h_kv <= 8.  ``scale`` defaults to
+    1/sqrt(D).  ``layout``: "auto", "general" or "fixed_block" (blocks of
+    ``block_keys`` keys, 0 = the library's choice).  A workspace of
+    gdn_attn_decode_workspace_size() bytes is allocated when none is given and
+    the layout may need one.  Returns o [B, h_q, D]."""
+    lib = _lib.load()
+    B, h_q, D = q.shape
+    h_kv, cap = k_cache.shape[1], k_cache.shape[2]
+    _require(k_cache.shape == (B, h_kv, cap, D) and v_cache.shape == k_cache.shape,
+             "k_cache / v_cache must be [B, h_kv, capacity, D]")
+    _require(cache_len.shape == (B,) and cache_len.dtype == torch.int32,
+             "cache_len must be [B] int32")
+    for t in (q, k_cache, v_cache, cache_len):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = D ** -0.5
+    if o is None:
+        o = torch.empty((B, h_q, D), dtype=q.dtype, device=q.device)
+    lay = _lib.ATTN_LAYOUTS[layout]
+    if workspace is None and layout != "general":
+        need = lib.gdn_attn_decode_workspace_size(B, h_q, h_kv, D, cap, lay, int(block_keys))
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.gdn_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), _ptr(o), B,
+                             h_q, h_kv, D, cap, dt, float(scale), lay, int(block_keys),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check(st, "gdn_attn_decode")
+    return o
 
 
 def gdn_stream_status(stream=None):

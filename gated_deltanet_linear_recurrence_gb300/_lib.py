@@ -14,11 +14,12 @@ STATUS_NAMES = {
     0: "GDN_OK", 1: "GDN_ERR_NULL_POINTER", 2: "GDN_ERR_INVALID_ARG",
     3: "GDN_ERR_UNSUPPORTED_SHAPE", 4: "GDN_ERR_UNSUPPORTED_DTYPE", 5: "GDN_ERR_MISALIGNED",
     6: "GDN_ERR_BAD_CU_SEQLENS", 7: "GDN_ERR_WORKSPACE_TOO_SMALL", 8: "GDN_ERR_DEVICE_TIMEOUT",
-    9: "GDN_ERR_CUDA",
+    9: "GDN_ERR_CUDA", 10: "GDN_ERR_BAD_CACHE_LEN",
 }
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OPT_QK_L2NORM = 1
 ALGOS = {"auto": 0, "scan": 1, "chunked": 2, "chunked_fused": 3, "chunked_split": 4}
+ATTN_LAYOUTS = {"auto": 0, "general": 1, "fixed_block": 2}
 
 # Exported symbols, with ctypes signatures: (restype, argtypes)
 _vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -46,6 +47,9 @@ SIGNATURES = {
     "gdn_decode_multi": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                         _i32, _i32, _i32, ctypes.c_int, _f32, ctypes.c_uint32,
                                         _vp]),
+    "gdn_attn_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                       ctypes.c_int, _f32, ctypes.c_int, _i32, _vp, _sz, _vp]),
+    "gdn_attn_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, ctypes.c_int, _i32]),
     "gdn_stream_status": (ctypes.c_int, [_vp]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_prefill_crossover_tokens": (_i32, [_i32, _i32, _i32, _i32, ctypes.c_int]),

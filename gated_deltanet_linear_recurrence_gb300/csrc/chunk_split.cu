@@ -93,14 +93,8 @@ __device__ __forceinline__ bool seq_range(const SplitParams& p, int n, int64_t& 
            (n == p.num_seqs - 1 && t1 != p.total_tokens));
 }
 
-// Programmatic dependent launch: the next kernel in the stream may start its
-// set-up now; and this kernel's reads of the previous kernel's results wait here.
-__device__ __forceinline__ void allow_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void wait_prerequisites() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+using tc::allow_dependents;
+using tc::wait_prerequisites;
 
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(256) chunk_plan_kernel(const SplitParams p) {

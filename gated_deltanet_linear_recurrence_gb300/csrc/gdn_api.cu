@@ -67,6 +67,23 @@ int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dt
   return kCrossoverTokens;
 }
 
+constexpr int32_t kAttnHeadDim = 256;
+constexpr int32_t kAttnMaxGroup = 8;
+constexpr int32_t kAttnMinBlock = 512;  // the smallest block the library picks
+
+gdn_status attn_shape(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim,
+                      int32_t capacity, int layout, int32_t block_keys) {
+  if (batch < 0 || capacity < 0 || h_q <= 0 || h_kv <= 0 || head_dim <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (layout < GDN_ATTN_AUTO || layout > GDN_ATTN_FIXED_BLOCK) return GDN_ERR_INVALID_ARG;
+  if (block_keys < 0 || block_keys % 64 != 0) return GDN_ERR_INVALID_ARG;
+  if (head_dim != kAttnHeadDim || h_q % h_kv != 0 || h_q / h_kv > kAttnMaxGroup)
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (batch > 65535 || h_kv > 65535 || (int64_t)batch * h_kv * capacity > INT32_MAX)
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -83,6 +100,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_WORKSPACE_TOO_SMALL: return "GDN_ERR_WORKSPACE_TOO_SMALL";
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_BAD_CACHE_LEN: return "GDN_ERR_BAD_CACHE_LEN";
   }
   return "GDN_ERR_UNKNOWN";
 }
@@ -268,6 +286,56 @@ gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const f
   a.dtype = dtype; a.scale = scale;
   a.qk_norm = (options & GDN_OPT_QK_L2NORM) ? 1 : 0;
   if (gdn::launch_decode_multi(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+size_t gdn_attn_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
+                                      int32_t head_dim, int32_t capacity,
+                                      gdn_attn_layout layout, int32_t block_keys) {
+  if (attn_shape(batch, h_q, h_kv, head_dim, capacity, layout, block_keys) != GDN_OK) return 0;
+  if (layout == GDN_ATTN_GENERAL) return 0;
+  const int64_t bk = block_keys > 0 ? block_keys : kAttnMinBlock;
+  const int64_t n = capacity > 0 ? (capacity + bk - 1) / bk : 1;
+  if (n <= 1) return 0;
+  return (size_t)batch * h_q * n * (head_dim + 2) * sizeof(float);
+}
+
+gdn_status gdn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* cache_len, void* o, int32_t batch, int32_t h_q,
+                           int32_t h_kv, int32_t head_dim, int32_t capacity, gdn_dtype dtype,
+                           float scale, gdn_attn_layout layout, int32_t block_keys,
+                           void* workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  gdn_status st = attn_shape(batch, h_q, h_kv, head_dim, capacity, layout, block_keys);
+  if (st != GDN_OK) return st;
+  if (dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  if (batch == 0) return GDN_OK;
+  if (!q || !o || !cache_len) return GDN_ERR_NULL_POINTER;
+  if (capacity > 0 && (!k_cache || !v_cache)) return GDN_ERR_NULL_POINTER;
+  const void* ptrs[] = {q, o, k_cache, v_cache, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) != 0) return GDN_ERR_MISALIGNED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::AttnPlan plan = gdn::attn_plan(batch, h_kv, capacity, layout, block_keys, sms);
+  size_t need = gdn::attn_partial_bytes(batch, h_q, plan);
+  if (need > 0 && (!workspace || workspace_bytes < need)) {
+    if (layout == GDN_ATTN_FIXED_BLOCK)
+      return workspace ? GDN_ERR_WORKSPACE_TOO_SMALL : GDN_ERR_NULL_POINTER;
+    plan = gdn::attn_plan(batch, h_kv, capacity, gdn::kAttnGeneral, 0, sms);  // AUTO: one block
+    need = 0;
+  }
+  gdn::AttnArgs a{};
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.cache_len = cache_len; a.o = o;
+  a.partial = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.batch = batch; a.h_q = h_q; a.h_kv = h_kv; a.head_dim = head_dim; a.capacity = capacity;
+  a.block_keys = plan.block_keys; a.n_split = plan.n_split; a.scale = scale;
+  st = error_word(&a.err);
+  if (st != GDN_OK) return st;
+  if (gdn::launch_attn_decode(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GDN_ERR_CUDA;
   return GDN_OK;
 }

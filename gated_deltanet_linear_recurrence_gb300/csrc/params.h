@@ -10,7 +10,7 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Device error codes written to the library's error word (same values as
 // gdn_status in include/gdn.h).
-enum DeviceError : int { kErrBadCuSeqlens = 6, kErrDeviceTimeout = 8 };
+enum DeviceError : int { kErrBadCuSeqlens = 6, kErrDeviceTimeout = 8, kErrBadCacheLen = 10 };
 
 struct DecodeArgs {
   const void* q;       // [B][h_k][d_k] dtype
@@ -69,7 +69,38 @@ struct PrefillArgs {
   int* err;                 // library error word on this device
 };
 
+// Grouped-query decode attention: q [B][h_q][D]; k_cache, v_cache
+// [B][h_kv][capacity][D]; cache_len [B] (device); o [B][h_q][D]; all bf16
+// except cache_len.  Each CTA takes block_keys cached keys of one (sequence,
+// KV head); with n_split > 1 it writes an unnormalised partial [acc[D], m, l]
+// per query head to `partial` [B][h_q][n_split][D + 2] and a combine pass
+// produces o.
+struct AttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* cache_len;
+  void* o;
+  float* partial;
+  int32_t batch, h_q, h_kv, head_dim, capacity;
+  int32_t block_keys, n_split;
+  float scale;
+  int* err;
+};
+
+// Decode-attention layouts (values of gdn_attn_layout) and the block plan:
+// general = one block spanning the cache; fixed-block = n_split equal blocks of
+// block_keys keys whose partial results a combine pass merges.
+enum AttnLayout : int { kAttnAuto = 0, kAttnGeneral = 1, kAttnFixedBlock = 2 };
+struct AttnPlan {
+  int32_t block_keys, n_split;
+};
+AttnPlan attn_plan(int32_t batch, int32_t h_kv, int32_t capacity, int layout, int32_t block_keys,
+                   int sm_count);
+size_t attn_partial_bytes(int32_t batch, int32_t h_q, const AttnPlan& plan);
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream);

@@ -66,7 +66,8 @@ typedef enum {
   GDN_ERR_BAD_CU_SEQLENS = 6,    /* device-detected: cu[0] != 0, decreasing, or cu[N] != T */
   GDN_ERR_WORKSPACE_TOO_SMALL = 7,
   GDN_ERR_DEVICE_TIMEOUT = 8,    /* device-detected: a bounded wait expired */
-  GDN_ERR_CUDA = 9               /* a CUDA runtime call failed */
+  GDN_ERR_CUDA = 9,              /* a CUDA runtime call failed */
+  GDN_ERR_BAD_CACHE_LEN = 10     /* device-detected: a cache_len outside 0 .. capacity */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype; /* dtype of q, k, v and o */
@@ -258,9 +259,71 @@ gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const f
                             uint32_t options, gdn_stream_t stream);
 
 /*
+ * gdn_attn_decode — grouped-query attention for one new token of each of
+ * `batch` sequences over its KV cache (the full-attention layers that sit
+ * between the recurrent layers of the same hybrid model).  Page "Optimizing
+ * on-device inference for Apple Silicon", section "Read the attention cache
+ * efficiently": the decode step reads the whole cache, so the kernel is bound
+ * by the bytes it reads; the query heads that share a KV head are served
+ * together so each cached row is read once ("Group query heads to reuse KV
+ * rows"); and at long context the cache is split into equal fixed blocks
+ * processed in parallel whose partial softmax results are then merged
+ * ("Switch attention layouts at long context", for heads of 256 values with
+ * eight query heads per KV head).
+ *
+ * For sequence b, query head h and its KV head j = h / (h_q / h_kv), over the
+ * L_b = cache_len[b] cached keys:
+ *     s_i = scale * (q_{b,h} . k_{b,j,i}),   o_{b,h} = sum_i softmax(s)_i v_{b,j,i}
+ * and o_{b,h} = 0 when L_b = 0.  Cache slots at or past L_b are never read into
+ * a result (they may hold anything, NaN included).
+ *
+ * Arguments: q [batch][h_q][head_dim], o [batch][h_q][head_dim], k_cache and
+ * v_cache [batch][h_kv][capacity][head_dim], all GDN_BF16 (else
+ * GDN_ERR_UNSUPPORTED_DTYPE); cache_len [batch] int32 device pointer with
+ * 0 <= cache_len[b] <= capacity (a value outside sets GDN_ERR_BAD_CACHE_LEN in
+ * the error word and that sequence gets o = 0).  head_dim must be 256 and
+ * h_q / h_kv an integer from 1 to 8, batch x h_kv x capacity below 2^31 (else
+ * GDN_ERR_UNSUPPORTED_SHAPE).  Pointers 16-byte aligned; k_cache and v_cache
+ * may be NULL only when capacity is 0.
+ *
+ * layout and block_keys: GDN_ATTN_GENERAL gives each (sequence, KV head) one
+ * CTA over its whole cache and writes o directly.  GDN_ATTN_FIXED_BLOCK splits
+ * the cache into blocks of block_keys keys (a positive multiple of 64, or 0 for
+ * a size the library picks from the SM count so that the blocks fill the GPU
+ * about once) processed by separate CTAs, then a combine pass merges their
+ * partial results through `workspace`; it needs workspace_bytes >=
+ * gdn_attn_decode_workspace_size(...) (else GDN_ERR_NULL_POINTER or
+ * GDN_ERR_WORKSPACE_TOO_SMALL).  GDN_ATTN_AUTO takes the fixed blocks when the
+ * (sequence, KV head) pairs are too few to fill the GPU and the workspace is
+ * large enough, else the general layout.  block_keys other than 0 or a
+ * positive multiple of 64 is GDN_ERR_INVALID_ARG.  The layouts agree within
+ * fp32 rounding of the softmax sums and the bf16 rounding of o.
+ */
+typedef enum {
+  GDN_ATTN_AUTO = 0,
+  GDN_ATTN_GENERAL = 1,
+  GDN_ATTN_FIXED_BLOCK = 2
+} gdn_attn_layout;
+
+gdn_status gdn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* cache_len, void* o, int32_t batch, int32_t h_q,
+                           int32_t h_kv, int32_t head_dim, int32_t capacity, gdn_dtype dtype,
+                           float scale, gdn_attn_layout layout, int32_t block_keys,
+                           void* workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Workspace bytes sufficient for gdn_attn_decode with these arguments, computed
+ * on the host: 0 for GDN_ATTN_GENERAL, else batch x h_q x n x (head_dim + 2) x
+ * 4 with n = ceil(capacity / block_keys), block_keys taken as 512 when 0 (the
+ * smallest block the library picks).  0 for invalid arguments. */
+size_t gdn_attn_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
+                                      int32_t head_dim, int32_t capacity,
+                                      gdn_attn_layout layout, int32_t block_keys);
+
+/*
  * gdn_stream_status — synchronise `stream`, then report (and clear) the
  * current device's error word: GDN_OK, GDN_ERR_BAD_CU_SEQLENS,
- * GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if the stream reported a CUDA error.
+ * GDN_ERR_BAD_CACHE_LEN, GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if the
+ * stream reported a CUDA error.
  */
 gdn_status gdn_stream_status(gdn_stream_t stream);
 

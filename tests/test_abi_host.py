@@ -181,3 +181,46 @@ def test_decode_multi_host_errors(lib):
     assert call(snap=FAKE + 16) == 2                     # snapshots overlap the state
     assert call(opts=2) == 2                             # unknown option bit
     assert call(b=0) == 0
+
+
+def attn(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, o=FAKE, b=1, h_q=16, h_kv=2, d=256, cap=4096,
+             dtype=1, scale=0.0625, layout=0, bk=0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.gdn_attn_decode(a["q"], a["k"], a["v"], a["lens"], a["o"], a["b"], a["h_q"],
+                               a["h_kv"], a["d"], a["cap"], a["dtype"], a["scale"], a["layout"],
+                               a["bk"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_attn_decode_host_errors(lib):
+    """Decode attention: every host-checkable error returns before any device call."""
+    assert attn(lib, q=None) == 1
+    assert attn(lib, lens=None) == 1
+    assert attn(lib, k=None) == 1                         # cache pointers needed when capacity > 0
+    assert attn(lib, b=-1) == 2
+    assert attn(lib, cap=-1) == 2
+    assert attn(lib, layout=3) == 2                       # bad enum
+    assert attn(lib, bk=100) == 2                         # not a multiple of 64
+    assert attn(lib, bk=-64) == 2
+    assert attn(lib, d=128) == 3                          # head dim 256 only
+    assert attn(lib, h_q=16, h_kv=3) == 3                 # h_q % h_kv
+    assert attn(lib, h_q=32, h_kv=2) == 3                 # more than 8 query heads per KV head
+    assert attn(lib, b=1024, h_kv=2, h_q=16, cap=1 << 21) == 3   # cache rows beyond int32
+    assert attn(lib, dtype=0) == 4                        # bf16 only
+    assert attn(lib, o=FAKE + 8) == 5
+    assert attn(lib, lens=FAKE + 2) == 5
+    assert attn(lib, b=0) == 0                            # nothing to do
+    assert attn(lib, b=0, q=None) == 0
+
+
+def test_attn_workspace_size(lib):
+    """Workspace bound: 0 for the general layout, else B x h_q x n x (D + 2) x 4
+    with n = ceil(capacity / block), block 512 when the library picks it."""
+    f = lib.gdn_attn_decode_workspace_size
+    assert f(1, 16, 2, 256, 131072, 1, 0) == 0
+    assert f(1, 16, 2, 256, 131072, 2, 2048) == 1 * 16 * 64 * 258 * 4
+    assert f(3, 16, 2, 256, 131072, 0, 0) == 3 * 16 * 256 * 258 * 4
+    assert f(2, 8, 1, 256, 1000, 2, 512) == 2 * 8 * 2 * 258 * 4
+    assert f(2, 8, 1, 256, 512, 2, 512) == 0              # a single block needs no merge
+    assert f(1, 16, 2, 128, 4096, 0, 0) == 0              # invalid shape
+    assert f(1, 16, 2, 256, 4096, 2, 100) == 0            # invalid block
