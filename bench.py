@@ -46,6 +46,9 @@ NCU_TRAFFIC = {
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
+    "attn_decode": {"files": ["attn_decode.cu", "tc.cuh", "rows.cuh"],
+                    "sha256_16": "b85689230fdf4243", "bytes": 268_529_664 + 3_432_192,
+                    "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh"],
                     "sha256_16": "5bd4e2fd057ca7a3", "bytes": 541_150_720 + 479_120_896,
                     "profile": "profiles/decode_step_b256.md"},
@@ -62,6 +65,20 @@ def ncu_traffic(kernel):
         with open(os.path.join(ROOT, "gated_deltanet_linear_recurrence_gb300", "csrc", f), "rb") as fh:
             m.update(fh.read())
     return rec["bytes"] if m.hexdigest()[:16] == rec["sha256_16"] else None
+
+
+def make_flush(torch, dev, l2):
+    """L2 flush between timed calls: write a buffer of twice the L2 size, then
+    read another one, so that no input of the next call is cached and no dirty
+    line of the flush is still waiting to be written back when the call starts."""
+    wbuf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()
+
+    return flush
 
 
 def load_peaks():
@@ -239,6 +256,7 @@ def main():
                     choices=["auto", "scan", "chunked", "chunked_fused", "chunked_split"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time the token scan and the chunked prefill over sequence lengths "
                          "(one sequence, 16 key / 32 value heads of 128, bf16) and print the "
@@ -246,7 +264,8 @@ def main():
     ap.add_argument("--stream", action="store_true",
                     help="time the 128K-token prompt as one call and as streamed pieces "
                          "(gdn_prefill_streamed), with the workspace each needs, as JSON lines")
-    ap.add_argument("--kernel-only", choices=["prefill", "decode_b256"], default=None,
+    ap.add_argument("--kernel-only", choices=["prefill", "decode_b256", "attn_b1_l131072",
+                                              "attn_b64_l8192"], default=None,
                     help="run only this kernel's workload (warmup + steps launches, no JSON); "
                          "for profiler captures")
     args = ap.parse_args()
@@ -298,10 +317,7 @@ def main():
     algo_used = args.algo if args.algo != "auto" else ("chunked" if T >= cross else "scan")
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-
-    def flush():
-        flush_buf.fill_(1)
+    flush = make_flush(torch, dev, l2)
 
     def prefill_once():
         gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], state_in=None,
@@ -432,6 +448,10 @@ def main():
     if not args.no_decode:
         decode = bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush)
 
+    attention = None
+    if not args.no_attention:
+        attention = bench_attention(torch, inputs, dev, stream, peaks, args, flush)
+
     clk = clocks.stop()
     assert gdn_stream_status(stream) == "GDN_OK"
 
@@ -444,13 +464,16 @@ def main():
                    "global_batch": world, "seq_len": T,
                    "parallelism": (f"{world} ranks, one prompt each (sequence shards, no "
                                    "exchange)") if world > 1 else "single GPU",
-                   "algo": algo_used, "l2": "flushed between timed steps (2x L2 buffer written)"},
+                   "algo": algo_used,
+                   "l2": ("flushed between timed steps: a 2x L2 buffer written, then another "
+                          "read, so no input is cached and no dirty line is pending")},
         "roofline": roof,
         "prefill_qk_l2norm": qk_variant,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
         "clocks": clk,
         "decode": decode,
+        "attn_decode": attention,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, w)
@@ -595,13 +618,92 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
     return out
 
 
+def attn_bytes(lengths, h_q, h_kv, head_dim):
+    """Algorithmic bytes of one decode-attention call: every cached K and V row of
+    every sequence once (bf16), q in and o out, and the lengths."""
+    cache = sum(lengths) * h_kv * head_dim * 2 * 2
+    return cache + 2 * len(lengths) * h_q * head_dim * 2 + 4 * len(lengths)
+
+
+def attn_device_inputs(torch, inputs, dev, name):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_attention(w["batch"], w["h_q"], w["h_kv"], w["head_dim"], w["capacity"],
+                              w["lengths"], w["dtype"], seed=w["seed"], poison_tail=False)
+    return w, {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def bench_attention(torch, inputs, dev, stream, peaks, args, flush):
+    """Decode attention of the full-attention layers (gdn_attn_decode): the
+    library's layout choice, and the general layout beside it, timed with CUDA
+    events on the launching stream, L2 flushed before each call."""
+    from gated_deltanet_linear_recurrence_gb300 import (gdn_attn_decode,
+                                                        gdn_attn_decode_block_keys)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(max(args.steps, 10)):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def measure(x, layout, lengths):
+        B, h_q, D = x["q"].shape
+        h_kv, cap = x["k_cache"].shape[1], x["k_cache"].shape[2]
+        o = torch.empty_like(x["q"])
+        ms = timed(lambda: gdn_attn_decode(x["q"], x["k_cache"], x["v_cache"], x["cache_len"],
+                                           o=o, layout=layout, stream=stream))
+        nbytes = attn_bytes(lengths, h_q, h_kv, D)
+        bk = gdn_attn_decode_block_keys(B, h_q, h_kv, D, cap, layout)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"us": ms * 1e3, "bytes": nbytes, "gbs": gbs,
+                "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "layout": layout,
+                "block_keys": bk, "blocks_per_kv_head": -(-cap // bk)}
+
+    out = {}
+    w, x = attn_device_inputs(torch, inputs, dev, "attn_b1_l131072")
+    head = measure(x, "auto", w["lengths"])
+    out["attn_b1_l131072"] = head
+    out["roofline"] = {"bound": "hbm", "achieved": head["gbs"], "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": head["gbs"] / peaks["hbm_gbs"],
+                       "traffic": ncu_traffic("attn_decode"),
+                       "scope": "the whole gdn_attn_decode call (attention kernel + combine)",
+                       "peak_source": f"{peaks['source']} copy bandwidth",
+                       "algorithmic_bytes_per_call": head["bytes"]}
+    # the pages' layout question at batch 1: general vs fixed blocks over contexts
+    sweep = []
+    for L in (4096, 32768, 131072):
+        xs = x if L == w["capacity"] else {
+            "q": x["q"], "k_cache": x["k_cache"][:, :, :L].contiguous(),
+            "v_cache": x["v_cache"][:, :, :L].contiguous(),
+            "cache_len": torch.full_like(x["cache_len"], L)}
+        gen = measure(xs, "general", [L])
+        fix = measure(xs, "fixed_block", [L])
+        sweep.append({"keys": L, "general_us": gen["us"], "fixed_block_us": fix["us"],
+                      "fixed_block_keys": fix["block_keys"],
+                      "fixed_vs_general": gen["us"] / fix["us"]})
+        del xs
+    out["layouts_b1"] = sweep
+    del x
+    w, x = attn_device_inputs(torch, inputs, dev, "attn_b64_l8192")
+    out["attn_b64_l8192"] = measure(x, "auto", w["lengths"])
+    del x
+    return out
+
+
 def run_sweep(args):
     """Scan vs chunked prefill time over sequence lengths (L2 flushed before each call)."""
     import torch
     from gated_deltanet_linear_recurrence_gb300 import gdn_prefill, gdn_stream_status, inputs
 
     dev = torch.device("cuda", 0)
-    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = make_flush(torch, dev, torch.cuda.get_device_properties(dev).L2_cache_size)
     lengths = [8, 16, 32, 64, 128, 256, 384, 512, 768, 1024, 2048, 4096, 8192, 16384, 65536,
                131072]
     rows = []
@@ -615,7 +717,7 @@ def run_sweep(args):
             reps = 3 if (algo == "scan" and T >= 16384) else 7
             ts = []
             for i in range(reps + 2):
-                flush_buf.fill_(1)
+                flush()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
@@ -647,7 +749,7 @@ def run_stream(args):
                                                         gdn_stream_status, inputs)
 
     dev = torch.device("cuda", 0)
-    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = make_flush(torch, dev, torch.cuda.get_device_properties(dev).L2_cache_size)
     w = inputs.WORKLOADS["prefill_t131072"]
     d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
                             seed=w["seed"], state_std=w["state_std"])
@@ -664,7 +766,7 @@ def run_stream(args):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         ts = []
         for i in range(args.warmup + 5):
-            flush_buf.fill_(1)
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             if piece is None:
@@ -693,7 +795,13 @@ def run_kernel_only(args):
                                                         gdn_stream_status, inputs)
 
     dev = torch.device("cuda", 0)
-    if args.kernel_only == "decode_b256":
+    if args.kernel_only.startswith("attn_"):
+        from gated_deltanet_linear_recurrence_gb300 import gdn_attn_decode
+        _, x = attn_device_inputs(torch, inputs, dev, args.kernel_only)
+        o = torch.empty_like(x["q"])
+        for _ in range(args.warmup + args.steps):
+            gdn_attn_decode(x["q"], x["k_cache"], x["v_cache"], x["cache_len"], o=o)
+    elif args.kernel_only == "decode_b256":
         w = inputs.WORKLOADS["decode_b256"]
         d = inputs.make_decode(w["batch"], w["h_k"], w["h_v"], w["d_k"], w["d_v"], w["dtype"],
                                seed=w["seed"])

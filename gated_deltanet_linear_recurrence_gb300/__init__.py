@@ -14,7 +14,7 @@ from ._lib import GdnError, STATUS_NAMES
 
 __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
            "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi", "gdn_attn_decode",
-           "gdn_attn_decode_workspace_size",
+           "gdn_attn_decode_workspace_size", "gdn_attn_decode_block_keys",
            "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
@@ -234,6 +234,14 @@ def gdn_attn_decode_workspace_size(batch, h_q, h_kv, head_dim, capacity, layout=
     return int(_lib.load().gdn_attn_decode_workspace_size(batch, h_q, h_kv, head_dim, capacity,
                                                           _lib.ATTN_LAYOUTS[layout],
                                                           int(block_keys)))
+
+
+def gdn_attn_decode_block_keys(batch, h_q, h_kv, head_dim, capacity, layout="auto",
+                               block_keys=0):
+    """Keys per CTA block that gdn_attn_decode would use on the current device (-1 if invalid)."""
+    return int(_lib.load().gdn_attn_decode_block_keys(batch, h_q, h_kv, head_dim, capacity,
+                                                      _lib.ATTN_LAYOUTS[layout],
+                                                      int(block_keys)))
 
 
 def gdn_attn_decode(q, k_cache, v_cache, cache_len, scale=None, o=None, layout="auto",

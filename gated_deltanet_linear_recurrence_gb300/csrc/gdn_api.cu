@@ -301,6 +301,17 @@ size_t gdn_attn_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   return (size_t)batch * h_q * n * (head_dim + 2) * sizeof(float);
 }
 
+int32_t gdn_attn_decode_block_keys(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim,
+                                   int32_t capacity, gdn_attn_layout layout,
+                                   int32_t block_keys) {
+  if (attn_shape(batch, h_q, h_kv, head_dim, capacity, layout, block_keys) != GDN_OK) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return gdn::attn_plan(batch, h_kv, capacity, layout, block_keys, sms).block_keys;
+}
+
 gdn_status gdn_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* cache_len, void* o, int32_t batch, int32_t h_q,
                            int32_t h_kv, int32_t head_dim, int32_t capacity, gdn_dtype dtype,

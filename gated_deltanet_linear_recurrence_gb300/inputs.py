@@ -134,6 +134,15 @@ WORKLOADS = {
     "prefill_varlen10": dict(kind="prefill", lengths=[256 << m for m in range(10)], h_k=16,
                              h_v=32, d_k=128, d_v=128, dtype="bf16", state_std=0.0,
                              seed=SEED_BASE + 5),
+    # decode attention of the hybrid model's full-attention layers (16 query heads on
+    # 2 KV heads of 256): one sequence's new token over a 128K-key cache
+    "attn_b1_l131072": dict(kind="attention", batch=1, h_q=16, h_kv=2, head_dim=256,
+                            capacity=131072, lengths=[131072], dtype="bf16",
+                            seed=SEED_BASE + 6),
+    # the same layer for 64 sequences of 8K cached keys each
+    "attn_b64_l8192": dict(kind="attention", batch=64, h_q=16, h_kv=2, head_dim=256,
+                           capacity=8192, lengths=[8192] * 64, dtype="bf16",
+                           seed=SEED_BASE + 7),
 }
 
 

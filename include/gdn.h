@@ -319,6 +319,15 @@ size_t gdn_attn_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
                                       int32_t head_dim, int32_t capacity,
                                       gdn_attn_layout layout, int32_t block_keys);
 
+/* The block of keys each CTA takes in gdn_attn_decode with these arguments on
+ * the current device, given a large enough workspace (capacity, or at least 1,
+ * for the general layout); -1 for invalid arguments or when the device cannot
+ * be queried.  The call launches ceil(capacity / result) CTAs per (sequence,
+ * KV head). */
+int32_t gdn_attn_decode_block_keys(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim,
+                                   int32_t capacity, gdn_attn_layout layout,
+                                   int32_t block_keys);
+
 /*
  * gdn_stream_status — synchronise `stream`, then report (and clear) the
  * current device's error word: GDN_OK, GDN_ERR_BAD_CU_SEQLENS,
