@@ -40,8 +40,8 @@ FP32_LANES_PER_SM = 128
 # the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "0fe1f9896bdaa1ee",
-                    "bytes": 5_376 + (68_257_024 + 28_667_392) + (119_578_112 + 12_312_832),
+                    "sha256_16": "b79e70d3e986c4bd",
+                    "bytes": 5_632 + (68_260_096 + 28_653_312) + (119_579_904 + 12_384_256),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
