@@ -148,20 +148,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // ------------------------------------------------------------------ prepare
 constexpr int kPrepThreads = 128;  // 4 warps; 4 CTAs per SM (TMEM, registers, shared memory)
 constexpr uint32_t kBarAll = 1, kBarGateP = 2;
+constexpr float kFactorRange = 80.f;  // |gamma| bound for Gamma_r / Gamma_i (e^80 < 2^127)
 // Shared memory of the prepare kernel, reused as the item advances:
 //   [0, 32K)     per d_k half kb: [Q 8K][K 8K] (TMA); after G: Q1 holds the
 //                solve scratch, then T diag(b Gamma); after W: K holds V (TMA)
 //   [32K, 49K)   A, then T: fp32 [64][kLdM]; then T diag(b) (bf16) at its start
-//   gates        Gamma[64], decay[64], Gamma_n, then gamma[64], beta[64], and the
-//                reciprocal L2 norms of the chunk's k rows and q rows (1 without
-//                the normalisation option)
+//   gates        Gamma[64], decay[64], the mask column factors |k_i|^-1 / Gamma_i [64],
+//                gamma[64], beta[64], the reciprocal L2 norms of the chunk's k rows
+//                and q rows (1 without the normalisation option), and a flag: the
+//                chunk's gamma range allows the factorised masks
 constexpr uint32_t PP_KQ = 0;
 constexpr uint32_t PP_Q1 = 16384;                  // solve scratch, then T diag(b Gamma)
 constexpr uint32_t PP_V = 8192;                    // V halves over K0 and K1 (stride 16K)
 constexpr uint32_t PP_MF = 32768;
 constexpr uint32_t PP_TA = PP_MF;                  // T diag(b), once T is in registers
 constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;
-constexpr uint32_t PP_MISC = PP_GATE + 7 * 64 * 4;
+constexpr uint32_t PP_MISC = PP_GATE + 7 * 64 * 4 + 16;  // + the factorisation flag
 constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
 static_assert(4 * (kPrepSmem + 1024) <= 233472, "four prepare CTAs per SM");
 constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W, then U~ (0-127)
@@ -201,8 +203,8 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   float* MF = reinterpret_cast<float*>(smem + PP_MF);
   float* YF = reinterpret_cast<float*>(smem + PP_Q1);
   float* gsm = reinterpret_cast<float*>(smem + PP_GATE);
-  float *Gam = gsm, *dec = gsm + 64, *gam = gsm + 192, *bet = gsm + 256;
-  float *rk = gsm + 320, *rq = gsm + 384;
+  float *Gam = gsm, *dec = gsm + 64, *cf = gsm + 128, *gam = gsm + 192, *bet = gsm + 256;
+  float *rk = gsm + 320, *rq = gsm + 384, *fact_flag = gsm + 448;
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);  // Q, K
   uint64_t* bar_mma = bar_tma + 1;
   uint64_t* bar_v = bar_tma + 2;                                     // V (needed only for U~)
@@ -285,10 +287,26 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       tc::named_sync(kBarGateP, 64);
       if (pw == 1) x += MF[0];
       gam[pt] = x;
-      Gam[pt] = tc::fast_exp(x);
+      const float Gx = tc::fast_exp(x);
+      Gam[pt] = Gx;
       bet[pt] = br;
+      float lo = x, hi = x;  // range of gamma over the chunk
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(kFullMask, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(kFullMask, hi, off));
+      }
+      if (lane == 0) {
+        MF[2 + pw] = lo;
+        MF[4 + pw] = hi;
+      }
       tc::named_sync(kBarGateP, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
+      // exp(gamma_r - gamma_i) = Gamma_r / Gamma_i without overflow or underflow
+      // while every gamma of the chunk lies in [-kFactorRange, kFactorRange]
+      const bool fact = fminf(MF[2], MF[3]) >= -kFactorRange && fmaxf(MF[4], MF[5]) <= kFactorRange;
+      cf[pt] = fact ? rk[pt] / Gx : 0.f;
+      if (pt == 0) *fact_flag = fact ? 1.f : 0.f;
     }
     ok = tc::mbar_wait(bar_mma, 0);
     tc::fence_after_sync();
@@ -302,46 +320,61 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   }
   if (ok) {
     // masks, one G row per thread (TMEM lane pt): P rows (warps 0, 1) to the
-    // package, A rows (warps 2, 3) to MF; 32 columns at a time
+    // package, A rows (warps 2, 3) to MF; 32 columns at a time.  Rows 0-31 have
+    // no entry in columns 32-63 (above the diagonal).  The decay factor
+    // exp(gamma_r - gamma_i) is the product of a row and a column factor when
+    // the chunk's gamma range allows it (one exponential per element otherwise).
     const int r = 32 * (pw & 1) + lane;
     const float g_r = gam[r], b_r = bet[r];
     const float n_r = pw < 2 ? rq[r] : rk[r];  // q_r for P rows, k_r for A rows
+    const bool fact = *fact_flag != 0.f;
+    const float rowf = (pw < 2 ? 1.f : b_r) * Gam[r] * n_r;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
       const int i0 = 32 * half;
       float a[32];
-      tc::tmem_ld32(tmem + lane_base + i0, a);
-      if (pw < 2) {
+      const bool above = (pw & 1) == 0 && half == 1;  // warp-uniform
+      if (above) {
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-          const float4 ki = *reinterpret_cast<const float4*>(rk + i0 + 4 * e4);
-          const float gv[4] = {gi.x, gi.y, gi.z, gi.w}, kv[4] = {ki.x, ki.y, ki.z, ki.w};
+        for (int e = 0; e < 32; ++e) a[e] = 0.f;
+      } else {
+        tc::tmem_ld32(tmem + lane_base + i0, a);
+        const int lim = pw < 2 ? r : r - 1;  // P keeps i <= r, A keeps i < r
+        if (fact) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int e = 4 * e4 + q, i = i0 + e;
-            a[e] = (i <= r) ? tc::fast_exp(g_r - gv[q]) * a[e] * (n_r * kv[q]) : 0.f;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(cf + i0 + 4 * e4);
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int e = 4 * e4 + q;
+              a[e] = (i0 + e <= lim) ? (a[e] * cv[q]) * rowf : 0.f;
+            }
+          }
+        } else {
+          const float bf = pw < 2 ? 1.f : b_r;
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
+            const float4 ki = *reinterpret_cast<const float4*>(rk + i0 + 4 * e4);
+            const float gv[4] = {gi.x, gi.y, gi.z, gi.w}, kv[4] = {ki.x, ki.y, ki.z, ki.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int e = 4 * e4 + q;
+              a[e] = (i0 + e <= lim) ? bf * tc::fast_exp(g_r - gv[q]) * a[e] * (n_r * kv[q]) : 0.f;
+            }
           }
         }
+      }
+      if (pw < 2) {
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
           st_chunk<3>(pkg + kPkgP, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
       } else {
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 gi = *reinterpret_cast<const float4*>(gam + i0 + 4 * e4);
-          const float4 ki = *reinterpret_cast<const float4*>(rk + i0 + 4 * e4);
-          const float gv[4] = {gi.x, gi.y, gi.z, gi.w}, kv[4] = {ki.x, ki.y, ki.z, ki.w};
-          float o4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = i0 + 4 * e4 + q;
-            o4[q] = (i < r) ? b_r * tc::fast_exp(g_r - gv[q]) * a[4 * e4 + q] * (n_r * kv[q])
-                            : 0.f;
-          }
+        for (int e4 = 0; e4 < 8; ++e4)
           *reinterpret_cast<float4*>(MF + r * kLdM + i0 + 4 * e4) =
-              make_float4(o4[0], o4[1], o4[2], o4[3]);
-        }
+              make_float4(a[4 * e4], a[4 * e4 + 1], a[4 * e4 + 2], a[4 * e4 + 3]);
       }
     }
     tc::fence_before_sync();
