@@ -40,8 +40,8 @@ FP32_LANES_PER_SM = 128
 # the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "b79e70d3e986c4bd",
-                    "bytes": 5_632 + (68_260_096 + 28_653_312) + (119_579_904 + 12_384_256),
+                    "sha256_16": "bd3582f17f9676a5",
+                    "bytes": 6_144 + (68_256_512 + 28_761_088) + (119_576_064 + 12_355_072),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
@@ -71,8 +71,9 @@ def make_flush(torch, dev, l2):
     """L2 flush between timed calls: write a buffer of twice the L2 size, then
     read another one, so that no input of the next call is cached and no dirty
     line of the flush is still waiting to be written back when the call starts."""
-    wbuf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    rbuf = torch.ones(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    n = max(2 * l2, 256 << 20)
+    wbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(n // 4, dtype=torch.float32, device=dev)  # summed by one reduction kernel
 
     def flush():
         wbuf.fill_(1)
