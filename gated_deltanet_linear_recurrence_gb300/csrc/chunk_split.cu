@@ -170,77 +170,72 @@ constexpr uint32_t kPrepTmemCols = 128;  // G (cols 0-63), then W, then U~ (0-12
 constexpr uint32_t IDP_G = tc::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDP_W = tc::idesc_bf16_f32(64, 128, false, true);
 
-__global__ void __launch_bounds__(kPrepThreads, 4)
-    chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31;
-  const int64_t item = blockIdx.x;
+// The sequence n and chunk c of package item `item` (chunk-major: item = chunk
+// id * h_v + value head); false past the last chunk.
+__device__ __forceinline__ bool item_chunk(const SplitParams& p, int64_t item, int& n, int& c) {
   const int64_t cid = item / p.h_v;
-  const int h = (int)(item % p.h_v);
-  // The chain kernel may launch once every CTA of this grid has started; its
-  // CTAs need an SM with room, so they start as this grid drains.
-  allow_dependents();
-  wait_prerequisites();  // the chunk table of the plan kernel
-  const int32_t total_chunks = p.chunk_base[p.num_seqs];
-  if (cid >= total_chunks) return;
+  if (cid >= p.chunk_base[p.num_seqs]) return false;
   // the sequence owning chunk cid: last n with chunk_base[n] <= cid (skipping empty ones)
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (p.chunk_base[mid] <= cid) lo = mid; else hi = mid - 1;
   }
-  const int n = lo;
-  const int c = (int)(cid - p.chunk_base[n]);
+  n = lo;
+  c = (int)(cid - p.chunk_base[n]);
+  return true;
+}
+
+// Thread 0 of a prepare item issues the copies of its chunk's Q and K rows
+// (key head of value head h) into the item's shared memory; bars[0] counts them.
+__device__ __forceinline__ void prepare_loads(const SplitParams& p, const CUtensorMap* tm_q,
+                                              const CUtensorMap* tm_k, uint8_t* smem,
+                                              uint64_t* bars, int64_t item, int n, int c) {
+  const int h = (int)(item % p.h_v);
+  const int hk = h / (p.h_v / p.h_k);
+  const int32_t y = static_cast<int32_t>(p.cu[n] + (int64_t)c * kC);
+  tc::mbar_arrive_expect_tx(bars, 32768);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    tc::tma_load_2d(smem + PP_KQ + kb * 16384, tm_q, hk * kDK + 64 * kb, y, bars);
+    tc::tma_load_2d(smem + PP_KQ + kb * 16384 + 8192, tm_k, hk * kDK + 64 * kb, y, bars);
+  }
+}
+
+// One prepare item (chunk, value head) on 128 threads (pt = 0..127) with the
+// shared-memory layout above at `smem`, 128 TMEM columns at `tmem`, three
+// mbarriers `bars` (Q/K landed, an MMA done, V landed; initialised with count 1)
+// that have seen k earlier items, and the named barriers kBA (128 threads) and
+// kBG (threads 0-63); prepare_loads has been issued for it.  Writes the item's
+// package; false if a wait expired.
+template <uint32_t kBA, uint32_t kBG>
+__device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtensorMap* tm_v,
+                                             uint8_t* smem, uint32_t tmem, uint64_t* bars,
+                                             uint32_t k, int pt, int64_t item, int n, int c) {
+  const int pw = pt >> 5, lane = pt & 31;
+  const int h = (int)(item % p.h_v);
   const int64_t t_beg = p.cu[n], t_end = p.cu[n + 1];
   const int64_t t0 = t_beg + (int64_t)c * kC;
-  const int hk = h / (p.h_v / p.h_k);
   uint8_t* pkg = p.packages + item * (int64_t)kPkgBytes;
-
   float* MF = reinterpret_cast<float*>(smem + PP_MF);
   float* YF = reinterpret_cast<float*>(smem + PP_Q1);
   float* gsm = reinterpret_cast<float*>(smem + PP_GATE);
   float *Gam = gsm, *dec = gsm + 64, *cf = gsm + 128, *gam = gsm + 192, *bet = gsm + 256;
   float *rk = gsm + 320, *rq = gsm + 384, *fact_flag = gsm + 448;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + PP_MISC);  // Q, K
-  uint64_t* bar_mma = bar_tma + 1;
-  uint64_t* bar_v = bar_tma + 2;                                     // V (needed only for U~)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 3);
+  uint64_t* bar_tma = bars;      // Q, K
+  uint64_t* bar_mma = bars + 1;
+  uint64_t* bar_v = bars + 2;    // V (needed only for U~)
   const uint32_t sbase = tc::smem_u32(smem);
   const int32_t y = static_cast<int32_t>(t0);
-
-  if (pw == 0) {
-    tc::tmem_alloc(tmem_slot, kPrepTmemCols);
-    tc::tmem_relinquish();
-  }
-  if (pt == 0) {
-    tc::mbar_init(bar_tma, 1);
-    tc::mbar_init(bar_mma, 1);
-    tc::mbar_init(bar_v, 1);
-    tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(bar_tma, 32768);
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load_2d(smem + PP_KQ + kb * 16384, &tm_q, hk * kDK + 64 * kb, y, bar_tma);
-      tc::tma_load_2d(smem + PP_KQ + kb * 16384 + 8192, &tm_k, hk * kDK + 64 * kb, y, bar_tma);
-    }
-  }
   float gr = 0.f, br = 0.f;
   if (pt < kC && t0 + pt < t_end) {
     gr = p.g[(t0 + pt) * p.h_v + h];
     br = p.beta[(t0 + pt) * p.h_v + h];
   }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
-  bool ok = tc::mbar_wait(bar_tma, 0);
+  bool ok = tc::mbar_wait(bar_tma, k & 1);
   tc::fence_after_sync();
-  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  ok = tc::named_sync_and(kBA, kPrepThreads, ok);
   if (ok) {
     if (pt == 64) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
 #pragma unroll
@@ -284,7 +279,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         if (lane >= off) x += yv;
       }
       if (pt == 31) MF[0] = x;
-      tc::named_sync(kBarGateP, 64);
+      tc::named_sync(kBG, 64);
       if (pw == 1) x += MF[0];
       gam[pt] = x;
       const float Gx = tc::fast_exp(x);
@@ -300,7 +295,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         MF[2 + pw] = lo;
         MF[4 + pw] = hi;
       }
-      tc::named_sync(kBarGateP, 64);
+      tc::named_sync(kBG, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
       // exp(gamma_r - gamma_i) = Gamma_r / Gamma_i without overflow or underflow
       // while every gamma of the chunk lies in [-kFactorRange, kFactorRange]
@@ -308,9 +303,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       cf[pt] = fact ? rk[pt] / Gx : 0.f;
       if (pt == 0) *fact_flag = fact ? 1.f : 0.f;
     }
-    ok = tc::mbar_wait(bar_mma, 0);
+    ok = tc::mbar_wait(bar_mma, (3 * k) & 1);
     tc::fence_after_sync();
-    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
     if (pt < 64) {  // the chain's per-row factors: Gamma_r / |q_r| for the output, decay_r / |k_r|
       float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
       gout[pt] = Gam[pt] * rq[pt];
@@ -378,10 +373,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
     }
     tc::fence_before_sync();
-    tc::named_sync(kBarAll, kPrepThreads);
+    tc::named_sync(kBA, kPrepThreads);
     tc::fence_after_sync();
 
-    unit_lower_inverse<kBarAll, kPrepThreads>(MF, YF, pt, lane);
+    unit_lower_inverse<kBA, kPrepThreads>(MF, YF, pt, lane);
 
     {  // T diag(b Gamma) over Q1 (W operand), T diag(b) over the start of MF (U~ operand)
       const int rr = pt >> 1, q = pt & 1;  // row rr, columns 32 q .. 32 q + 31
@@ -391,7 +386,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         const float4 m = *reinterpret_cast<const float4*>(MF + rr * kLdM + 32 * q + 4 * e4);
         t[4 * e4] = m.x; t[4 * e4 + 1] = m.y; t[4 * e4 + 2] = m.z; t[4 * e4 + 3] = m.w;
       }
-      tc::named_sync(kBarAll, kPrepThreads);  // every row of T is read before TA overwrites MF
+      tc::named_sync(kBA, kPrepThreads);  // every row of T is read before TA overwrites MF
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         const int ii = 32 * q + 8 * c8;
@@ -407,7 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    tc::named_sync(kBarAll, kPrepThreads);
+    tc::named_sync(kBA, kPrepThreads);
     tc::fence_after_sync();
     if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
 #pragma unroll
@@ -417,9 +412,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
                      IDP_W, kk > 0);
       tc::mma_commit(bar_mma);
     }
-    ok = tc::mbar_wait(bar_mma, 1);
+    ok = tc::mbar_wait(bar_mma, (3 * k + 1) & 1);
     tc::fence_after_sync();
-    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
   }
   if (ok) {
     if (pt == 0) {  // K is consumed: V (two 64-column boxes) over K0 and K1
@@ -429,7 +424,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       // never written
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
-        tc::tma_load_2d(smem + PP_V + kb * 16384, &tm_v, h * p.d_v + 64 * kb, y, bar_v);
+        tc::tma_load_2d(smem + PP_V + kb * 16384, tm_v, h * p.d_v + 64 * kb, y, bar_v);
     }
     // -W (M=64 accumulator: row 16 w + lane on lanes 0-15) to the package
     const int r = 16 * pw + lane;
@@ -447,9 +442,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
     }
     tc::fence_before_sync();
-    tc::named_sync(kBarAll, kPrepThreads);  // W's columns are read before U~ overwrites them
+    tc::named_sync(kBA, kPrepThreads);  // W's columns are read before U~ overwrites them
     tc::fence_after_sync();
-    if (pt == 64 && tc::mbar_wait(bar_v, 0)) {  // (on a timeout nothing commits: all time out)
+    if (pt == 64 && tc::mbar_wait(bar_v, k & 1)) {  // (on a timeout nothing commits: all time out)
       tc::fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V: M=64 N=128 K=64
@@ -458,9 +453,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
                      kk > 0);
       tc::mma_commit(bar_mma);
     }
-    ok = tc::mbar_wait(bar_mma, 0);
+    ok = tc::mbar_wait(bar_mma, (3 * k + 2) & 1);
     tc::fence_after_sync();
-    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
     if (ok) {  // U~ slices (bf16, 64-byte rows with the SW64 XOR pattern) to the package
 #pragma unroll 1
       for (int sl = 0; sl < 4; ++sl) {
@@ -473,102 +468,153 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
     }
   }
+  return ok;
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 4)
+    chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int pt = threadIdx.x;
+  const int64_t item = blockIdx.x;
+  // The chain kernel may launch once every CTA of this grid has started; its
+  // CTAs need an SM with room, so they start as this grid drains.
+  allow_dependents();
+  wait_prerequisites();  // the chunk table of the plan kernel
+  int n, c;
+  if (!item_chunk(p, item, n, c)) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PP_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
+  if (pt < 32) {
+    tc::tmem_alloc(tmem_slot, kPrepTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (pt == 0) {
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+    tc::fence_mbar_init();
+    prepare_loads(p, &tm_q, &tm_k, smem, bars, item, n, c);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool ok = prepare_item<kBarAll, kBarGateP>(p, &tm_v, smem, *tmem_slot, bars,
+                                                   0, pt, item, n, c);
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (pw == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
+  if (pt < 32) tc::tmem_dealloc(*tmem_slot, kPrepTmemCols);
 }
 
 // ------------------------------------------------------------------ chain
-constexpr int kChainThreads = 128;                       // epilogue warps 0-3
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kChainKernelThreads = kChainThreads + 64;  // + producer and MMA warps
-constexpr int kStages = 3;
+constexpr uint32_t kBarChainCta = 3;                     // named barrier of a chain's threads
 // Main stage: per d_k half kb [-W | Q | K] (8 KB each; [-W; Q] is one 128-row
-// operand), then the slice's U~ (4 KB); released once the chunk's state update
-// is done.  Tail stage: P (8 KB) and the gates, released after the chunk's
+// operand), then the CTA's U~ slices (4 KB per 32 values); released once the
+// chunk's state update is done.  Tail stage: P (8 KB) and, in a ring of their
+// own after the other buffers, the chunk's gates; released after the chunk's
 // output (one chunk later).  The 64 rows before each P are valid shared
 // memory, as an M=128 operand whose other half is never read.
 constexpr uint32_t kHalf = 24576;
 constexpr uint32_t SC_W = 0, SC_Q = 8192, SC_K = 16384, SC_U = 2 * kHalf;
-constexpr uint32_t kMain = SC_U + kPkgUSlice;                              // 53248
-constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + kPkgUSlice;
-static_assert(kMainTx == kMain, "every main-stage byte arrives by TMA or bulk copy");
-constexpr uint32_t TL_P = 0, TL_G = 8192;
-constexpr uint32_t kTail = 9216;
-constexpr uint32_t kTailTx = 8192 + 1024;
-constexpr uint32_t CC_TAIL = kStages * kMain;
-constexpr uint32_t CC_SS = CC_TAIL + kStages * kTail;    // S slice bf16 [j][i], SW64, 8 KB
-constexpr uint32_t CC_UB = CC_SS + 8192;                 // U bf16 [r][i], SW64
-constexpr uint32_t CC_UK = CC_UB + 4096;                 // decayed U bf16 [r][i], SW64
-constexpr uint32_t CC_MISC = CC_UK + 4096;
-constexpr uint32_t kChainSmem = CC_MISC + 256 + 1024;
-static_assert(kChainSmem <= 227 * 1024, "shared memory budget");
-static_assert(kMain % 1024 == 0 && kTail % 1024 == 0 && CC_TAIL % 1024 == 0 &&
-                  CC_SS % 1024 == 0 && SC_U % 512 == 0,
-              "swizzled operands need 1024 / 512 byte alignment");
-constexpr uint32_t kChainTmemCols = 256;
-constexpr uint32_t TC_D0 = 0, TC_O0 = 64, TC_S = 128;  // D and P U double-buffered
-constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, 32, false, true);  // [-W; Q] S^T
-constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, 32, true, true);   // K^T (decay U)
-constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, 32, false, true);  // [.; P] U (rows 64-127)
+constexpr uint32_t kTail = 8192;      // P
+constexpr uint32_t kGateBytes = 528;  // the package's gates: Gamma q[64], decay k[64], Gamma_n
+constexpr uint32_t kTailTx = kTail + kGateBytes;
 
+// A chain CTA that owns DVS (32 or 64) rows of a head's state (value dims),
+// runs NSTG pipeline stages and EW epilogue warps (4, or 8 for DVS = 64: warps w
+// and w + 4 share TMEM lanes 32 (w % 4) .. and take one 32-value block each).
+// Operands of 32 values per row are SW64 blocks; DVS = 64 uses two blocks side
+// by side (the MMA descriptors' leading offset).
+template <int DVS, int NSTG, int EW = 4>
+struct ChainCfg {
+  static constexpr int NB = DVS / 32;
+  static constexpr int BPW = NB * 4 / EW;  // 32-value blocks per epilogue warp
+  static constexpr int kThreads = 32 * EW + 64;
+  static constexpr int kProducerWarp = EW, kMmaWarp = EW + 1;
+  static constexpr int kStages = NSTG, kEW = EW;
+  static constexpr uint32_t kMain = SC_U + NB * kPkgUSlice;
+  static constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + NB * kPkgUSlice;
+  static constexpr uint32_t CC_TAIL = NSTG * kMain;
+  static constexpr uint32_t CC_SS = CC_TAIL + NSTG * kTail;  // S^T bf16 [j][i]: NB x [128][32]
+  static constexpr uint32_t CC_UB = CC_SS + NB * 8192;       // U bf16 [r][i]: NB x [64][32]
+  static constexpr uint32_t CC_UK = CC_UB + NB * 4096;       // decayed U, same layout
+  static constexpr uint32_t CC_GATE = CC_UK + NB * 4096;    // NSTG x kGateBytes
+  static constexpr uint32_t CC_MISC = CC_GATE + NSTG * kGateBytes;
+  static constexpr uint32_t kSmem = CC_MISC + 256 + 1024;
+  static constexpr uint32_t kTmemCols = DVS == 32 ? 256 : 512;
+  static constexpr uint32_t TC_D0 = 0, TC_O0 = 2 * DVS, TC_S = 4 * DVS;  // D, P U double-buffered
+  static constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, DVS, false, true);  // [-W; Q] S^T
+  static constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, DVS, true, true);   // K^T (decay U)
+  static constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, DVS, false, true);  // [.; P] U
+  static_assert(DVS == 32 || DVS == 64, "32 or 64 state rows per CTA");
+  static_assert((EW == 4 || EW == 8) && BPW >= 1, "4 or 8 epilogue warps, at most one per block");
+  static_assert(kMainTx == kMain, "every main-stage byte arrives by TMA or bulk copy");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kMain % 1024 == 0 && kTail % 1024 == 0 && CC_TAIL % 1024 == 0 &&
+                    CC_SS % 1024 == 0 && SC_U % 512 == 0,
+                "swizzled operands need 1024 / 512 byte alignment");
+  static_assert(5 * DVS <= (int)kTmemCols, "TMEM columns");
+};
 
-__global__ void __launch_bounds__(kChainKernelThreads, 1)
-    chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ns = p.d_v / kDVS;
-  const int s = blockIdx.x % ns;
-  const int h = (blockIdx.x / ns) % p.h_v;
-  const int n = blockIdx.x / (ns * p.h_v);
+// The sequential state pass of one (sequence n, value head h, DVS-row slice s)
+// on ChainCfg::kThreads threads: EW epilogue warps, a producer warp and an MMA
+// warp.
+template <int DVS, int NSTG, int EW>
+__device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMap* tm_q,
+                                          const CUtensorMap* tm_k, uint8_t* smem, int n, int h,
+                                          int s, int tid) {
+  using CF = ChainCfg<DVS, NSTG, EW>;
+  constexpr int BPW = CF::BPW;
+  constexpr int kEpiThreads = 32 * EW;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int b0 = (warp >> 2) * BPW;      // first 32-value block of an epilogue warp
+  const int jrow = 32 * (warp & 3) + lane;  // its TMEM lane: row of S^T (key dim)
   const int hk = h / (p.h_v / p.h_k);
   int64_t t_beg, t_end;
   if (!seq_range(p, n, t_beg, t_end)) return;  // reported by the plan kernel
   const int64_t L = t_end - t_beg;
   if (L < p.min_len) return;  // the token scan owns this sequence
   const int nchunks = (int)((L + kC - 1) / kC);
-  const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * kDVS;
+  const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * DVS;
 
   // mbarriers.  full/tfull: TMA and bulk copies landed; empty: the stage's MMAs
   // are done (tcgen05.commit); tempty: warps 2-3 wrote the chunk's output.
   // bar_d, bar_s, bar_o: D, the state update, P U complete (tcgen05.commit);
   // bar_u: warps 0-1 staged U; bar_ss: warps 0-3 staged the state.
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CC_MISC);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + kStages;
-  uint64_t* bar_d = tempty + kStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CF::CC_MISC);
+  uint64_t* empty = full + NSTG;
+  uint64_t* tfull = empty + NSTG;
+  uint64_t* tempty = tfull + NSTG;
+  uint64_t* bar_d = tempty + NSTG;
   uint64_t* bar_s = bar_d + 1;
   uint64_t* bar_u = bar_s + 1;
   uint64_t* bar_ss = bar_u + 1;
   uint64_t* bar_o = bar_ss + 1;  // one per chunk parity
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, kChainTmemCols);
+    tc::tmem_alloc(tmem_slot, CF::kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < NSTG; ++i) {
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], 1);
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 64);
+      tc::mbar_init(&tempty[i], 2 * kEpiThreads / 4);
     }
     tc::mbar_init(bar_d, 1);
     tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_u, 64);
-    tc::mbar_init(bar_ss, kChainThreads);
+    tc::mbar_init(bar_u, 2 * kEpiThreads / 4);
+    tc::mbar_init(bar_ss, kEpiThreads);
     tc::mbar_init(&bar_o[0], 1);
     tc::mbar_init(&bar_o[1], 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  tc::named_sync(kBarChainCta, CF::kThreads);
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = tc::smem_u32(smem);
@@ -577,35 +623,35 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
   wait_prerequisites();  // the packages and chunk table (set-up above overlapped the prepare)
   const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
 
-  if (warp == kProducerWarp) {
+  if (warp == CF::kProducerWarp) {
     if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(tm_q);
+      tc::prefetch_tmap(tm_k);
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c % kStages;
-        const uint8_t* pkg = p.packages + (first_item + (int64_t)c * p.h_v) * kPkgBytes;
-        if (c >= kStages) ok = tc::mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+        const int st = c % NSTG;
+        const int64_t item = first_item + (int64_t)c * p.h_v;
+        const uint8_t* pkg = p.packages + item * kPkgBytes;
+        if (c >= NSTG) ok = tc::mbar_wait(&empty[st], ((c / NSTG) - 1) & 1);
         if (!ok) break;
-        uint8_t* dst = smem + st * kMain;
+        uint8_t* dst = smem + st * CF::kMain;
         const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
         uint64_t* fb = &full[st];
-        tc::mbar_arrive_expect_tx(fb, kMainTx);
+        tc::mbar_arrive_expect_tx(fb, CF::kMainTx);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          tc::tma_load_2d(dst + kb * kHalf + SC_Q, &tm_q, hk * kDK + 64 * kb, y, fb);
-          tc::tma_load_2d(dst + kb * kHalf + SC_K, &tm_k, hk * kDK + 64 * kb, y, fb);
+          tc::tma_load_2d(dst + kb * kHalf + SC_Q, tm_q, hk * kDK + 64 * kb, y, fb);
+          tc::tma_load_2d(dst + kb * kHalf + SC_K, tm_k, hk * kDK + 64 * kb, y, fb);
           bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
         }
-        bulk_g2s(dst + SC_U, pkg + kPkgU + s * kPkgUSlice, kPkgUSlice, fb);
-        if (c >= kStages) ok = tc::mbar_wait(&tempty[st], ((c / kStages) - 1) & 1);
+        bulk_g2s(dst + SC_U, pkg + kPkgU + s * CF::NB * kPkgUSlice, CF::NB * kPkgUSlice, fb);
+        if (c >= NSTG) ok = tc::mbar_wait(&tempty[st], ((c / NSTG) - 1) & 1);
         if (!ok) break;
-        uint8_t* tl = smem + CC_TAIL + st * kTail;
         tc::mbar_arrive_expect_tx(&tfull[st], kTailTx);
-        bulk_g2s(tl + TL_P, pkg + kPkgP, 8192, &tfull[st]);
-        bulk_g2s(tl + TL_G, pkg + kPkgGates, 1024, &tfull[st]);
+        bulk_g2s(smem + CF::CC_TAIL + st * kTail, pkg + kPkgP, 8192, &tfull[st]);
+        bulk_g2s(smem + CF::CC_GATE + st * kGateBytes, pkg + kPkgGates, kGateBytes, &tfull[st]);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == CF::kMmaWarp) {
     // Issues every tensor-core product, in the order the chain needs them.  The
     // whole warp runs the loop converged: every lane waits on the barrier
     // itself, and one elected lane issues the MMAs and commits.  (Measured on
@@ -619,23 +665,25 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
     };
     // Operand descriptors built once; a stage or K step only adds its byte
     // offset / 16 to the start-address field (every address is below 256 KB).
-    const uint64_t dSS = tc::smem_desc(sbase + CC_SS, 4096, 512, tc::kLayoutSw64);
-    const uint64_t dUK = tc::smem_desc(sbase + CC_UK, 4096, 512, tc::kLayoutSw64);
-    const uint64_t dUB = tc::smem_desc(sbase + CC_UB, 4096, 512, tc::kLayoutSw64);
+    // The leading byte offset steps between the 32-value blocks (DVS = 64).
+    const uint64_t dSS = tc::smem_desc(sbase + CF::CC_SS, 8192, 512, tc::kLayoutSw64);
+    const uint64_t dUK = tc::smem_desc(sbase + CF::CC_UK, 4096, 512, tc::kLayoutSw64);
+    const uint64_t dUB = tc::smem_desc(sbase + CF::CC_UB, 4096, 512, tc::kLayoutSw64);
     const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
     const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
-    const uint64_t dP0 = tc::smem_desc(sbase + CC_TAIL + TL_P - 8192, 16, 1024, tc::kLayoutSw128);
+    const uint64_t dP0 =
+        tc::smem_desc(sbase + CF::CC_TAIL - 8192, 16, 1024, tc::kLayoutSw128);
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % kStages;
-      const uint64_t so = (uint64_t)((st * kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
+      const int st = c % NSTG;
+      const uint64_t so = (uint64_t)((st * CF::kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
       const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
-      const uint32_t td = tmem + TC_D0 + 32 * (c & 1), to2 = tmem + TC_O0 + 32 * (c & 1);
-      if (!(ok = warp_wait(&full[st], (c / kStages) & 1) && warp_wait(bar_ss, c & 1))) break;
+      const uint32_t td = tmem + CF::TC_D0 + DVS * (c & 1), to2 = tmem + CF::TC_O0 + DVS * (c & 1);
+      if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
       if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // D = [-W; Q] S_s^T
           tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
-                       dSS + ((kk * 1024) >> 4), IDC_WQ, kk > 0);
+                       dSS + ((kk * 1024) >> 4), CF::IDC_WQ, kk > 0);
         tc::mma_commit(bar_d);
       }
       __syncwarp();
@@ -643,53 +691,57 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
-          tc::mma_bf16(tmem + TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4), IDC_SU, 1);
+          tc::mma_bf16(tmem + CF::TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4),
+                       CF::IDC_SU, 1);
         tc::mma_commit(bar_s);
         tc::mma_commit(&empty[st]);  // -W, Q, K and U~ of the stage consumed
       }
       __syncwarp();
-      if (!(ok = warp_wait(&tfull[st], (c / kStages) & 1))) break;
+      if (!(ok = warp_wait(&tfull[st], (c / NSTG) & 1))) break;
       if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
-          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), IDC_PU, kk > 0);
+          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), CF::IDC_PU, kk > 0);
         tc::mma_commit(&bar_o[c & 1]);
       }
       __syncwarp();
     }
-  } else {
-    // Epilogue warps.  Warps 0-1 (TMEM lanes 0-63) form U; warps 2-3 (lanes
-    // 64-127) write the previous chunk's output meanwhile; all four stage the
-    // state.  Every hand-off is an mbarrier with a bounded wait.
+  } else if (warp < EW) {
+    // Epilogue warps.  Those on TMEM lanes 0-63 form U; those on lanes 64-127
+    // write the previous chunk's output meanwhile; all stage the state.  Every
+    // hand-off is an mbarrier with a bounded wait.
     const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
     // Output of chunk cp (warps 2-3): O = Gamma Q S^T + P U for rows r = lanes
     // 64-127, then release its tail stage.
     auto finish_output = [&](int cp) {
-      const int stp = cp % kStages;
-      const float* gp = reinterpret_cast<const float*>(smem + CC_TAIL + stp * kTail + TL_G);
+      const int stp = cp % NSTG;
+      const float* gp = reinterpret_cast<const float*>(smem + CF::CC_GATE + stp * kGateBytes);
       // P U of chunk cp + 2 is issued only after this chunk's output is done
       // (warps 2-3 then stage chunk cp + 1's state), so the parity is unambiguous
       ok = tc::mbar_wait(&bar_o[cp & 1], (cp >> 1) & 1) && ok;
       tc::fence_after_sync();
       const int64_t t0p = t_beg + (int64_t)cp * kC;
       const int nvp = (int)((L - (int64_t)cp * kC) < kC ? (L - (int64_t)cp * kC) : kC);
-      float o1[32], o2[32];
-      tc::tmem_ld32(tmem + lane_base + TC_D0 + 32 * (cp & 1), o1);
-      tc::tmem_ld32(tmem + lane_base + TC_O0 + 32 * (cp & 1), o2);
-      if (rl < nvp) {
-        const float Gam_r = gp[rl];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0p + rl) * p.h_v + h) * (int64_t)p.d_v +
-                                              s * kDVS);
+      for (int b = b0; b < b0 + BPW; ++b) {
+        float o1[32], o2[32];
+        tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (cp & 1) + 32 * b, o1);
+        tc::tmem_ld32(tmem + lane_base + CF::TC_O0 + DVS * (cp & 1) + 32 * b, o2);
+        if (rl < nvp) {
+          const float Gam_r = gp[rl];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint4 q4;
-          q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
-          q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
-          q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
-          q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
-          dst[c4] = q4;
+          for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0p + rl) * p.h_v + h) * (int64_t)p.d_v +
+                                                s * DVS + 32 * b);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint4 q4;
+            q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
+            q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
+            q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
+            q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
+            dst[c4] = q4;
+          }
         }
       }
       tc::fence_before_sync();
@@ -698,61 +750,74 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
     // S (fp32, thread j holds column j of the slice) -> bf16 operand copy for
     // chunk cn's D, then Gamma_n of chunk cn applied in TMEM (the update MMA
     // accumulates onto it); then tell the MMA warp.
-    auto stage_state = [&](float (&sc)[32], int cn) {
+    auto stage_state = [&](float (&sc)[32 * BPW], int cn) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_SS, tid * 64 + c4 * 16, sc + 8 * c4);
-      const int stn = cn % kStages;
-      ok = tc::mbar_wait(&tfull[stn], (cn / kStages) & 1) && ok;
-      const float Gam_n = reinterpret_cast<const float*>(smem + CC_TAIL + stn * kTail + TL_G)[128];
+      for (int b = 0; b < BPW; ++b)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
-      tc::tmem_st32(tmem + lane_base + TC_S, sc);
+        for (int c4 = 0; c4 < 4; ++c4)
+          st_chunk<2>(smem + CF::CC_SS + (b0 + b) * 8192, jrow * 64 + c4 * 16, sc + 32 * b + 8 * c4);
+      const int stn = cn % NSTG;
+      ok = tc::mbar_wait(&tfull[stn], (cn / NSTG) & 1) && ok;
+      const float Gam_n =
+          reinterpret_cast<const float*>(smem + CF::CC_GATE + stn * kGateBytes)[128];
+#pragma unroll
+      for (int i = 0; i < 32 * BPW; ++i) sc[i] *= Gam_n;
+#pragma unroll
+      for (int b = 0; b < BPW; ++b)
+        tc::tmem_st32(tmem + lane_base + CF::TC_S + 32 * (b0 + b),
+                      *reinterpret_cast<const float(*)[32]>(sc + 32 * b));
       tc::fence_proxy_async();
       tc::fence_before_sync();
       tc::mbar_arrive(bar_ss);
     };
-    {  // initial state
-      float sc[32];
+    {  // initial state: rows 32 b0 .. of the slice, column jrow
+      float sc[32 * BPW];
 #pragma unroll
-      for (int i = 0; i < kDVS; ++i)
-        sc[i] = p.state_in ? p.state_in[(srow0 + i) * kDK + tid] : 0.f;
+      for (int i = 0; i < 32 * BPW; ++i)
+        sc[i] = p.state_in ? p.state_in[(srow0 + 32 * b0 + i) * kDK + jrow] : 0.f;
       if (nchunks == 0) {
 #pragma unroll
-        for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+        for (int i = 0; i < 32 * BPW; ++i) p.state_out[(srow0 + 32 * b0 + i) * kDK + jrow] = sc[i];
       } else {
         stage_state(sc, 0);
       }
     }
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % kStages;
-      const float* gates = reinterpret_cast<const float*>(smem + CC_TAIL + st * kTail + TL_G);
-      if (warp < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
+      const int st = c % NSTG;
+      const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
+      if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
         ok = tc::mbar_wait(bar_d, c & 1) && ok;
         // U~ arrived by bulk copy: observe the stage's own barrier before reading it
-        ok = tc::mbar_wait(&full[st], (c / kStages) & 1) && ok;
+        ok = tc::mbar_wait(&full[st], (c / NSTG) & 1) && ok;
         tc::fence_after_sync();
         const float dec_r = gates[64 + rl];
-        float u[32], d[32];
-        tc::tmem_ld32(tmem + lane_base + TC_D0 + 32 * (c & 1), d);
-        const uint8_t* ut = smem + st * kMain + SC_U;  // this row of U~, bf16
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 q4 = *reinterpret_cast<const uint4*>(ut + tc::swizzle<2>(rl * 64 + j * 16));
-          const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+        for (int b = b0; b < b0 + BPW; ++b) {
+          float u[32], d[32];
+          tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c & 1) + 32 * b, d);
+          const uint8_t* ut = smem + st * CF::kMain + SC_U + b * kPkgUSlice;  // row of U~, bf16
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            u[8 * j + 2 * e] = __uint_as_float(w4[e] << 16);
-            u[8 * j + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 q4 =
+                *reinterpret_cast<const uint4*>(ut + tc::swizzle<2>(rl * 64 + j * 16));
+            const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              u[8 * j + 2 * e] = __uint_as_float(w4[e] << 16);
+              u[8 * j + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] += d[i];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            st_chunk<2>(smem + CF::CC_UB + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] *= dec_r;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            st_chunk<2>(smem + CF::CC_UK + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
         }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] += d[i];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_UB, rl * 64 + c4 * 16, u + 8 * c4);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] *= dec_r;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) st_chunk<2>(smem + CC_UK, rl * 64 + c4 * 16, u + 8 * c4);
         tc::fence_proxy_async();
         tc::fence_before_sync();
         tc::mbar_arrive(bar_u);
@@ -761,22 +826,43 @@ __global__ void __launch_bounds__(kChainKernelThreads, 1)
       }
       ok = tc::mbar_wait(bar_s, c & 1) && ok;
       tc::fence_after_sync();
-      float sc[32];
-      tc::tmem_ld32(tmem + lane_base + TC_S, sc);
+      float sc[32 * BPW];
+#pragma unroll
+      for (int b = 0; b < BPW; ++b)
+        tc::tmem_ld32(tmem + lane_base + CF::TC_S + 32 * (b0 + b),
+                      *reinterpret_cast<float(*)[32]>(sc + 32 * b));
       if (c == nchunks - 1) {
 #pragma unroll
-        for (int i = 0; i < kDVS; ++i) p.state_out[(srow0 + i) * kDK + tid] = sc[i];
+        for (int i = 0; i < 32 * BPW; ++i) p.state_out[(srow0 + 32 * b0 + i) * kDK + jrow] = sc[i];
       } else {
         stage_state(sc, c + 1);
       }
     }
-    if (ok && nchunks > 0 && warp >= 2) finish_output(nchunks - 1);  // the last chunk's output
+    if (ok && nchunks > 0 && (warp & 3) >= 2) finish_output(nchunks - 1);  // the last output
   }
   if (!ok) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
-  __syncthreads();
+  tc::named_sync(kBarChainCta, CF::kThreads);
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, kChainTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tmem, CF::kTmemCols);
+}
+
+// The chain of the two-kernel form: 32 state rows per CTA, 3 stages, 4 epilogue warps.
+using SplitChain = ChainCfg<kDVS, 3, 4>;
+
+__global__ void __launch_bounds__(SplitChain::kThreads, 1)
+    chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  constexpr int kRows = SplitChain::NB * 32;
+  const int ns = p.d_v / kRows;
+  const int s = blockIdx.x % ns;
+  const int h = (blockIdx.x / ns) % p.h_v;
+  const int n = blockIdx.x / (ns * p.h_v);
+  chain_run<SplitChain::NB * 32, SplitChain::kStages, SplitChain::kEW>(p, &tm_q, &tm_k, smem, n, h,
+                                                                     s, threadIdx.x);
 }
 
 // ------------------------------------------------------------------ host side
@@ -830,7 +916,7 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kChainSmem);
+                               SplitChain::kSmem);
     return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -872,11 +958,11 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   cfg.dynamicSmemBytes = kPrepSmem;
   e = cudaLaunchKernelEx(&cfg, chunk_prepare_kernel, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
-  const int64_t grid = (int64_t)a.num_seqs * a.h_v * (a.d_v / kDVS);
+  const int64_t grid = (int64_t)a.num_seqs * a.h_v * (a.d_v / (SplitChain::NB * 32));
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kChainKernelThreads);
-  cfg.dynamicSmemBytes = kChainSmem;
+  cfg.blockDim = dim3(SplitChain::kThreads);
+  cfg.dynamicSmemBytes = SplitChain::kSmem;
   return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, mq, mk, p);
 }
 

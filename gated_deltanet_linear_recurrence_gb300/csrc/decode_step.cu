@@ -19,6 +19,7 @@
 
 #include "params.h"
 #include "rows.cuh"
+#include "tc.cuh"
 
 namespace gdn {
 namespace {
@@ -45,6 +46,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int lam = lane % L;
   const int hk = h / (h_v / h_k);
   const int64_t bh = (int64_t)b * h_v + h;
+  // Launched with programmatic stream serialization: the next kernel in the
+  // stream may be scheduled now, and every input is read only once the kernel
+  // before this one has completed.
+  tc::allow_dependents();
+  tc::wait_prerequisites();
 
   // state rows first: they are the bytes that matter
   float* srow = state + (bh * d_v + row0 + grp) * (int64_t)DK + 4 * lam;
@@ -103,12 +109,19 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   const int blocks_per_head = (a.d_v + rows_per_block - 1) / rows_per_block;
   const int64_t gx = (int64_t)a.batch * blocks_per_head;
   if (gx > 0x7fffffffLL || a.h_v > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)gx, (unsigned)a.h_v);
-  decode_step_kernel<DK, R, T><<<grid, kDecodeWarps * 32, 0, stream>>>(
-      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
-      a.beta, a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale,
-      a.qk_norm);
-  return cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)a.h_v);
+  cfg.blockDim = dim3(kDecodeWarps * 32);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<DK, R, T>, static_cast<const T*>(a.q),
+                            static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g, a.beta,
+                            a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head,
+                            a.scale, a.qk_norm);
 }
 
 // Rows per lane group: R = L/2 gives 16 rows per warp (most bytes in flight
