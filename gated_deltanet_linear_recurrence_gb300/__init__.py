@@ -13,6 +13,7 @@ from . import _lib
 from ._lib import GdnError, STATUS_NAMES
 
 __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
+           "gdn_prefill_host", "gdn_prefill_host_workspace_size",
            "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi", "gdn_attn_decode",
            "gdn_attn_decode_workspace_size", "gdn_attn_decode_block_keys",
            "gdn_prefill_workspace_size",
@@ -141,6 +142,47 @@ def gdn_prefill_streamed(q, k, v, g, beta, piece_tokens, state_in=None, state_ou
                                   float(scale), int(piece_tokens), _ptr(workspace), ws_bytes,
                                   _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_prefill_streamed")
+    return o, state_out
+
+
+def gdn_prefill_host_workspace_size(piece_tokens, h_k, h_v, d_k, d_v, dtype=torch.bfloat16):
+    return int(_lib.load().gdn_prefill_host_workspace_size(piece_tokens, h_k, h_v, d_k, d_v,
+                                                           _DTYPES[dtype]))
+
+
+def gdn_prefill_host(q, k, v, g, beta, piece_tokens=1024, state_in=None, state_out=None, o=None,
+                     scale=1.0, workspace=None, stream=None, qk_l2norm=False, device=None):
+    """gdn_prefill_host in include/gdn.h: one sequence whose tensors are on the HOST
+    (q, k [T, h_k, d_k]; v [T, h_v, d_v]; g, beta [T, h_v]; page-locked for overlap),
+    prefilled in pieces with the copies overlapped.  Outputs o [T, h_v, d_v] and
+    state_out [1, h_v, d_v, d_k] are host tensors (page-locked ones are allocated
+    when not given); a device workspace is allocated when none is given.  The
+    results are ready once the stream is synchronised.  Returns (o, state_out)."""
+    lib = _lib.load()
+    T, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    _require(k.shape == q.shape and v.shape[0] == T, "q/k/v shapes disagree")
+    _require(g.shape == (T, h_v) and beta.shape == (T, h_v), "g/beta must be [T, h_v]")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    for t in (q, k, v, g, beta, state_in):
+        _require(t is None or (t.device.type == "cpu" and t.is_contiguous()),
+                 "inputs must be contiguous host tensors")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((T, h_v, d_v), dtype=q.dtype).pin_memory()
+    if state_out is None:
+        state_out = torch.empty((1, h_v, d_v, d_k), dtype=torch.float32).pin_memory()
+    _require(o.device.type == "cpu" and state_out.device.type == "cpu", "outputs must be on the host")
+    if workspace is None:
+        need = lib.gdn_prefill_host_workspace_size(piece_tokens, h_k, h_v, d_k, d_v, dt)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=device if device is not None else "cuda")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                              _ptr(state_out), _ptr(o), T, h_k, h_v, d_k, d_v, dt, float(scale),
+                              int(piece_tokens), _ptr(workspace), ws_bytes, _options(qk_l2norm),
+                              _stream(stream))
+    _lib.check(st, "gdn_prefill_host")
     return o, state_out
 
 

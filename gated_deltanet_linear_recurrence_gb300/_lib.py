@@ -39,6 +39,10 @@ SIGNATURES = {
                                             _i32, _i32, _i32, ctypes.c_int, _f32, _i64, _vp, _sz,
                                             ctypes.c_uint32, _vp]),
     "gdn_prefill_streamed_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32, ctypes.c_int]),
+    "gdn_prefill_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32,
+                                        _i32, _i32, ctypes.c_int, _f32, _i64, _vp, _sz,
+                                        ctypes.c_uint32, _vp]),
+    "gdn_prefill_host_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32, ctypes.c_int]),
     "gdn_prefill_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                                            _i64, _i32, _i32, _i32, _i32, ctypes.c_int, _f32,
                                            _vp]),

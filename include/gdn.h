@@ -182,6 +182,40 @@ size_t gdn_prefill_streamed_workspace_size(int64_t piece_tokens, int32_t h_k, in
                                            int32_t d_k, int32_t d_v, gdn_dtype dtype);
 
 /*
+ * gdn_prefill_host — gdn_prefill_streamed for a sequence whose tensors live in
+ * HOST memory: q, k, v, g, beta, state_in (or NULL: zeros), state_out and o are
+ * host pointers with the layouts of gdn_prefill_streamed; workspace is DEVICE
+ * memory of at least gdn_prefill_host_workspace_size(piece_tokens, ...) bytes,
+ * 16-byte aligned.  The prompt is cut into pieces of piece_tokens tokens (a
+ * positive multiple of 64) and the copy of one piece's inputs to the device,
+ * the prefill of the previous piece and the copy of the piece before that back
+ * to the host overlap: the library orders them with two copy streams of its
+ * own and events, joined back into `stream` (graph capture works as for one
+ * stream).  The source pages have no host-side counterpart; it serves callers
+ * whose data is on the host, where copies, not the prefill, set the time.
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister): from
+ * pageable memory the driver stages each copy and nothing overlaps.
+ *
+ * Results equal gdn_prefill_streamed with the same piece size bit for bit and
+ * are complete in host memory when `stream` reaches the point after this call
+ * (synchronise it before reading them).  Calls on one device are serialised
+ * while they enqueue work.  Errors: those of gdn_prefill_streamed; host
+ * pointers are not checked beyond NULL.
+ */
+gdn_status gdn_prefill_host(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* state_in, float* state_out, void* o,
+                            int64_t total_tokens, int32_t h_k, int32_t h_v, int32_t d_k,
+                            int32_t d_v, gdn_dtype dtype, float scale, int64_t piece_tokens,
+                            void* workspace, size_t workspace_bytes, uint32_t options,
+                            gdn_stream_t stream);
+
+/* Device workspace bytes for gdn_prefill_host with pieces of piece_tokens
+ * tokens: two buffers of one piece's inputs and outputs, the state, and one
+ * piece's prefill workspace (0 for invalid arguments). */
+size_t gdn_prefill_host_workspace_size(int64_t piece_tokens, int32_t h_k, int32_t h_v,
+                                       int32_t d_k, int32_t d_v, gdn_dtype dtype);
+
+/*
  * gdn_prefill_noalloc — gdn_prefill with GDN_ALGO_CHUNKED_SPLIT (the
  * two-kernel chunked evaluation), taking its scratch from a fixed array of
  * GDN_NOALLOC_SCRATCH_BYTES that the library holds in device memory instead of

@@ -224,3 +224,33 @@ def test_attn_workspace_size(lib):
     assert f(2, 8, 1, 256, 512, 2, 512) == 0              # a single block needs no merge
     assert f(1, 16, 2, 128, 4096, 0, 0) == 0              # invalid shape
     assert f(1, 16, 2, 256, 4096, 2, 100) == 0            # invalid block
+
+
+def test_prefill_from_host_memory_errors(lib):
+    """gdn_prefill_host: host-checkable errors return before any device call."""
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, si=None, so=FAKE, o=FAKE, t=4096,
+                 h_k=16, h_v=32, d_k=128, d_v=128, dtype=1, scale=1.0, piece=1024, ws=FAKE,
+                 ws_bytes=1 << 40, opt=0, stream=None)
+        a.update(kw)
+        return lib.gdn_prefill_host(a["q"], a["k"], a["v"], a["g"], a["beta"], a["si"], a["so"],
+                                    a["o"], a["t"], a["h_k"], a["h_v"], a["d_k"], a["d_v"],
+                                    a["dtype"], a["scale"], a["piece"], a["ws"], a["ws_bytes"],
+                                    a["opt"], a["stream"])
+    assert call(piece=100) == 2                          # not a multiple of 64
+    assert call(piece=0) == 2
+    assert call(t=-1) == 2
+    assert call(opt=4) == 2                              # unknown option bit
+    assert call(dtype=7) == 4
+    assert call(d_k=48) == 3
+    assert call(h_k=3, h_v=32) == 3
+    assert call(q=None) == 1
+    assert call(so=None) == 1
+    assert call(ws=None) == 1
+    assert call(ws=FAKE + 8) == 5
+    assert call(ws_bytes=1024) == 7                      # workspace too small
+    need = lib.gdn_prefill_host_workspace_size(1024, 16, 32, 128, 128, 1)
+    assert need > 0 and call(ws_bytes=need - 1) == 7
+    assert lib.gdn_prefill_host_workspace_size(100, 16, 32, 128, 128, 1) == 0
+    # grows with the piece, not with the prompt
+    assert lib.gdn_prefill_host_workspace_size(2048, 16, 32, 128, 128, 1) > need
