@@ -40,8 +40,8 @@ FP32_LANES_PER_SM = 128
 # the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "bd3582f17f9676a5",
-                    "bytes": 6_144 + (68_256_512 + 28_761_088) + (119_576_064 + 12_355_072),
+                    "sha256_16": "8c6c1d8e790cc58d",
+                    "bytes": 6_144 + (68_259_072 + 29_017_600) + (118_790_912 + 12_413_440),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
@@ -49,8 +49,8 @@ NCU_TRAFFIC = {
     "attn_decode": {"files": ["attn_decode.cu", "tc.cuh", "rows.cuh"],
                     "sha256_16": "b85689230fdf4243", "bytes": 268_529_664 + 3_432_192,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
-    "decode_step": {"files": ["decode_step.cu", "rows.cuh"],
-                    "sha256_16": "5bd4e2fd057ca7a3", "bytes": 541_150_720 + 479_120_896,
+    "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
+                    "sha256_16": "aeafdf16e54526c5", "bytes": 541_154_304 + 479_891_712,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
