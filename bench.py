@@ -254,7 +254,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto",
-                    choices=["auto", "scan", "chunked", "chunked_fused", "chunked_split"])
+                    choices=["auto", "scan", "chunked", "chunked_fused", "chunked_split",
+                             "chunked_coop"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
@@ -382,8 +383,9 @@ def main():
     dq = inputs.make_prefill(lengths, h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + n0 + 1,
                              unit_qk=False)
     xq = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dq.items()}
+    ws_q_algo = args.algo if args.algo in ("chunked_split", "chunked_coop") else "chunked_split"
     ws_q = torch.empty(max(gdn_prefill_workspace_size(1, T, h_k, h_v, d_k, d_v, torch.bfloat16,
-                                                      "chunked_split"), 16),
+                                                      ws_q_algo), 16),
                        dtype=torch.uint8, device=dev)
 
     def prefill_qk():
@@ -763,7 +765,9 @@ def run_stream(args):
     o = torch.empty((T, w["h_v"], w["d_v"]), dtype=torch.bfloat16, device=dev)
     st = torch.empty((1, w["h_v"], w["d_v"], w["d_k"]), dtype=torch.float32, device=dev)
     shape = (w["h_k"], w["h_v"], w["d_k"], w["d_v"])
-    cases = [("whole", None, gdn_prefill_workspace_size(1, T, *shape, algo="chunked_split"))]
+    cases = [("whole", None, gdn_prefill_workspace_size(1, T, *shape, algo="chunked_split")),
+             ("whole, cooperative", "coop", gdn_prefill_workspace_size(1, T, *shape,
+                                                                        algo="chunked_coop"))]
     for piece in (2048, 8192, 32768):
         cases.append((f"pieces of {piece}", piece,
                       gdn_prefill_streamed_workspace_size(piece, *shape)))
@@ -774,9 +778,10 @@ def run_stream(args):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            if piece is None:
+            if piece is None or piece == "coop":
                 gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
-                            state_in=x["state_in"], state_out=st, o=o, algo="chunked_split",
+                            state_in=x["state_in"], state_out=st, o=o,
+                            algo="chunked_split" if piece is None else "chunked_coop",
                             workspace=ws)
             else:
                 gdn_prefill_streamed(x["q"], x["k"], x["v"], x["g"], x["beta"], piece,

@@ -71,7 +71,7 @@ def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=N
     q, k [T, h_k, d_k]; v [T, h_v, d_v] (fp32 or bf16); g, beta [T, h_v] fp32;
     cu_seqlens [N+1] int32 on the device; state_in [N, h_v, d_v, d_k] fp32 or
     None (zeros).  Returns (o [T, h_v, d_v], state_out [N, h_v, d_v, d_k]).
-    ``algo``: "auto", "scan", "chunked", "chunked_fused" or "chunked_split".
+    ``algo``: "auto", "scan", "chunked", "chunked_fused", "chunked_split" or "chunked_coop".
     ``qk_l2norm``: divide q and k by their per-head L2 norm inside the kernels.
     Without ``workspace`` one of the size gdn_prefill_workspace_size() reports
     is allocated (none when that is 0).

@@ -18,7 +18,8 @@ STATUS_NAMES = {
 }
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OPT_QK_L2NORM = 1
-ALGOS = {"auto": 0, "scan": 1, "chunked": 2, "chunked_fused": 3, "chunked_split": 4}
+ALGOS = {"auto": 0, "scan": 1, "chunked": 2, "chunked_fused": 3, "chunked_split": 4,
+         "chunked_coop": 5}
 ATTN_LAYOUTS = {"auto": 0, "general": 1, "fixed_block": 2}
 
 # Exported symbols, with ctypes signatures: (restype, argtypes)

@@ -559,13 +559,33 @@ struct ChainCfg {
   static_assert(5 * DVS <= (int)kTmemCols, "TMEM columns");
 };
 
+// Bounded wait for a prepare item's ready flag (stored with release semantics
+// by the CTA that wrote the package), then order it before this thread's bulk
+// copies of the package (async proxy).
+__device__ __forceinline__ bool wait_item_flag(const int* flag,
+                                               uint64_t timeout_ns = 200000000ull) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  if (v == 0) {
+    const uint64_t t0 = tc::globaltimer_ns();
+    do {
+      __nanosleep(100);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      if (v == 0 && tc::globaltimer_ns() - t0 > timeout_ns) return false;
+    } while (v == 0);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // The sequential state pass of one (sequence n, value head h, DVS-row slice s)
 // on ChainCfg::kThreads threads: EW epilogue warps, a producer warp and an MMA
-// warp.
+// warp.  With item_flags, a chunk's package is copied only once its flag is
+// set (its prepare item runs in another CTA of the same cooperative grid).
 template <int DVS, int NSTG, int EW>
 __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, uint8_t* smem, int n, int h,
-                                          int s, int tid) {
+                                          int s, int tid, const int* item_flags) {
   using CF = ChainCfg<DVS, NSTG, EW>;
   constexpr int BPW = CF::BPW;
   constexpr int kEpiThreads = 32 * EW;
@@ -632,6 +652,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         const int64_t item = first_item + (int64_t)c * p.h_v;
         const uint8_t* pkg = p.packages + item * kPkgBytes;
         if (c >= NSTG) ok = tc::mbar_wait(&empty[st], ((c / NSTG) - 1) & 1);
+        if (ok && item_flags) ok = wait_item_flag(item_flags + item);
         if (!ok) break;
         uint8_t* dst = smem + st * CF::kMain;
         const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
@@ -862,7 +883,7 @@ __global__ void __launch_bounds__(SplitChain::kThreads, 1)
   const int h = (blockIdx.x / ns) % p.h_v;
   const int n = blockIdx.x / (ns * p.h_v);
   chain_run<SplitChain::NB * 32, SplitChain::kStages, SplitChain::kEW>(p, &tm_q, &tm_k, smem, n, h,
-                                                                     s, threadIdx.x);
+                                                                     s, threadIdx.x, nullptr);
 }
 
 // ------------------------------------------------------------------ host side
@@ -893,15 +914,127 @@ bool encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------------------------ cooperative form
+// One grid with every CTA resident (cooperative launch, one CTA per SM).  The
+// first n_chain CTAs each run the chain of one (sequence, value head, 64-row
+// slice); the others run prepare items in four slots of 128 threads, in chunk
+// order, and store a ready flag per item once its package is written.  A
+// chain's producer waits for the flag before copying the package, so the
+// chain follows the prepare chunk by chunk instead of starting after all of it.
+// Waits go one way only (chain on prepare), and every CTA is resident, so the
+// grid cannot deadlock; each wait is bounded as well.
+using CoopChain = ChainCfg<64, 3, 8>;
+constexpr int kCoopSlots = 4;
+constexpr int kCoopThreads = kCoopSlots * kPrepThreads;
+constexpr uint32_t kPrepSlotBytes = (kPrepSmem - 1024 + 1023) / 1024 * 1024;
+constexpr uint32_t kCoopSmem = CoopChain::kSmem > kCoopSlots * kPrepSlotBytes + 1024
+                                   ? CoopChain::kSmem
+                                   : kCoopSlots * kPrepSlotBytes + 1024;
+static_assert(CoopChain::kThreads <= kCoopThreads, "the chain fits in the grid's CTAs");
+static_assert(kCoopSmem <= 227 * 1024, "shared memory budget");
+static_assert(kCoopSlots * kPrepTmemCols <= 512, "TMEM of the prepare slots");
+
+// One prepare slot: 128 threads with their own shared memory, TMEM, mbarriers
+// and named barriers kBA, kBG, taking items from a counter shared by all slots
+// (flags[max_items], zero at launch) in increasing order, i.e. chunk by chunk.
+template <uint32_t kBA, uint32_t kBG>
+__device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CUtensorMap* tm_q,
+                                                  const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                                  uint8_t* smem, int pt, int* flags) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PP_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
+  int* next = reinterpret_cast<int*>(bars + 4);  // the slot's item, from the shared counter
+  if (pt < 32) tc::tmem_alloc(tmem_slot, kPrepTmemCols);
+  if (pt == 0) {
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+    tc::fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  tc::named_sync(kBA, kPrepThreads);
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  uint32_t k = 0;
+  for (;; ++k) {
+    if (pt == 0) *next = atomicAdd(flags + p.max_items, 1);
+    tc::named_sync(kBA, kPrepThreads);
+    const int64_t item = *next;
+    int n, c;
+    if (!ok || item >= p.max_items || !item_chunk(p, item, n, c)) break;  // past the last chunk
+    if (pt == 0) prepare_loads(p, tm_q, tm_k, smem, bars, item, n, c);
+    ok = prepare_item<kBA, kBG>(p, tm_v, smem, tmem, bars, k, pt, item, n, c);
+    // Every thread's package stores are visible device-wide before the flag;
+    // the slot's shared memory and TMEM are free for the next item.
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    tc::named_sync(kBA, kPrepThreads);
+    tc::fence_after_sync();
+    if (pt == 0 && ok)
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flags + item), "r"(1) : "memory");
+  }
+  if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
+  tc::fence_before_sync();
+  tc::named_sync(kBA, kPrepThreads);
+  tc::fence_after_sync();
+  if (pt < 32) tc::tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+__global__ void __launch_bounds__(kCoopThreads, 1)
+    chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const SplitParams p, int n_chain,
+                      int* flags) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  if ((int)blockIdx.x < n_chain) {
+    if ((int)threadIdx.x >= CoopChain::kThreads) return;
+    constexpr int kRows = CoopChain::NB * 32;
+    const int ns = p.d_v / kRows;
+    const int s = blockIdx.x % ns;
+    const int h = (blockIdx.x / ns) % p.h_v;
+    const int n = blockIdx.x / (ns * p.h_v);
+    chain_run<kRows, CoopChain::kStages, CoopChain::kEW>(p, &tm_q, &tm_k, smem, n, h, s,
+                                                         threadIdx.x, flags);
+    return;
+  }
+  wait_prerequisites();  // the chunk table of the plan kernel
+  const int slot = threadIdx.x / kPrepThreads, pt = threadIdx.x % kPrepThreads;
+  uint8_t* sm = smem + slot * kPrepSlotBytes;
+  switch (slot) {
+    case 0: coop_prepare_slot<1, 2>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
+    case 1: coop_prepare_slot<3, 4>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
+    case 2: coop_prepare_slot<5, 6>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
+    default: coop_prepare_slot<7, 8>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
+  }
+}
+
 }  // namespace
 
 size_t split_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v) {
   return split_header_bytes(num_seqs) + split_max_items(num_seqs, total_tokens, h_v) * kPkgBytes;
 }
 
-cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv;  // mv: V in 64-column boxes for the prepare kernel's U~
+size_t coop_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v) {
+  // one ready flag per item and the item counter of the prepare slots
+  const size_t flags =
+      ((split_max_items(num_seqs, total_tokens, h_v) + 1) * sizeof(int) + 1023) / 1024 * 1024;
+  return split_workspace_bytes(num_seqs, total_tokens, h_v) + flags;
+}
+
+bool coop_supported(int32_t num_seqs, int32_t h_v, int32_t d_v, int sm_count) {
+  // 64-row chain slices; at least a third of the SMs left for the prepare slots
+  if (d_v % 64 != 0) return false;
+  const int64_t n_chain = (int64_t)num_seqs * h_v * (d_v / 64);
+  return n_chain >= 1 && n_chain <= (int64_t)sm_count * 2 / 3;
+}
+
+// Tensor maps (Q, K, V in 64-column boxes) and kernel parameters shared by the
+// two-kernel and the cooperative forms.
+bool split_setup(const PrefillArgs& a, void* workspace, CUtensorMap& mq, CUtensorMap& mk,
+                 CUtensorMap& mv, SplitParams& p) {
   const uint64_t rows = a.total_tokens > 0 ? (uint64_t)a.total_tokens : 1;
   const void* qp = a.total_tokens > 0 ? a.q : a.state_out;
   const void* kp = a.total_tokens > 0 ? a.k : a.state_out;
@@ -909,18 +1042,7 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   if (!encode_map(&mq, qp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mk, kp, (uint64_t)a.h_k * a.d_k, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mv, vp, (uint64_t)a.h_v * a.d_v, rows, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  static PerDeviceOnce attrs;
-  const cudaError_t attr_err = attrs.run([] {
-    cudaError_t e = cudaFuncSetAttribute(chunk_prepare_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SplitChain::kSmem);
-    return e;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  SplitParams p;
+    return false;
   p.g = a.g;
   p.beta = a.beta;
   p.state_in = a.state_in;
@@ -939,6 +1061,67 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   p.packages = static_cast<uint8_t*>(workspace) + split_header_bytes(a.num_seqs);
   p.max_items = (int64_t)split_max_items(a.num_seqs, a.total_tokens, a.h_v);
   p.err = a.err;
+  return true;
+}
+
+cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (!coop_supported(a.num_seqs, a.h_v, a.d_v, sms)) return cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv;
+  SplitParams p;
+  if (!split_setup(a, workspace, mq, mk, mv, p)) return cudaErrorInvalidValue;
+  if (p.max_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  static PerDeviceOnce attrs;
+  e = attrs.run([] {
+    return cudaFuncSetAttribute(chunk_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kCoopSmem);
+  });
+  if (e != cudaSuccess) return e;
+  int resident = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, chunk_coop_kernel, kCoopThreads,
+                                                    kCoopSmem);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorNotSupported;
+  int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                      split_workspace_bytes(a.num_seqs, a.total_tokens, a.h_v));
+  chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(flags, 0, (size_t)(p.max_items + 1) * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  const int n_chain = a.num_seqs * a.h_v * (a.d_v / 64);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(kCoopThreads);
+  cfg.dynamicSmemBytes = kCoopSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_coop_kernel, mq, mk, mv, p, n_chain, flags);
+}
+
+cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;  // mv: V in 64-column boxes for the prepare kernel's U~
+  SplitParams p;
+  if (!split_setup(a, workspace, mq, mk, mv, p)) return cudaErrorInvalidValue;
+  static PerDeviceOnce attrs;
+  const cudaError_t attr_err = attrs.run([] {
+    cudaError_t e = cudaFuncSetAttribute(chunk_prepare_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SplitChain::kSmem);
+    return e;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   // prepare and chain launch with programmatic stream serialization: each may

@@ -58,6 +58,14 @@ constexpr int32_t kCrossoverTokens = 16;
 // this many tokens and the caller's workspace is large enough.
 constexpr int64_t kSplitMinAvgTokens = 256;
 
+// Two kernels vs one cooperative kernel (prepare and chain overlapped in one
+// grid).  Same sweep, one sequence: the two kernels are faster at 2,048 tokens
+// (66.2 vs 80.7 us) and 4,096 (117.7 vs 123.5 us), the cooperative kernel from
+// 8,192 (213.6 vs 219.8 us; 1.42 vs 1.64 ms at 64K tokens, 2.78 vs 3.25 ms at
+// 128K).  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED use it from this average length
+// when its chains fit (coop_supported) and the workspace holds its flags.
+constexpr int64_t kCoopMinAvgTokens = 8192;
+
 bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
   return num_seqs > 0 && total_tokens >= kSplitMinAvgTokens * num_seqs;
 }
@@ -117,8 +125,10 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
   if (num_seqs < 0 || total_tokens < 0 || check_heads(h_k, h_v, d_k, d_v) != GDN_OK) return 0;
   if (algo == GDN_ALGO_SCAN || algo == GDN_ALGO_CHUNKED_FUSED) return 0;
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return 0;
-  if (algo != GDN_ALGO_CHUNKED_SPLIT && !split_preferred(num_seqs, total_tokens)) return 0;
-  return gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
+  if (algo == GDN_ALGO_CHUNKED_SPLIT) return gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
+  if (algo != GDN_ALGO_CHUNKED_COOP && !split_preferred(num_seqs, total_tokens)) return 0;
+  // AUTO and CHUNKED: room for the cooperative form (the two-kernel form plus flags)
+  return gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v);
 }
 
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
@@ -141,7 +151,8 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
   if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED &&
-      algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT)
+      algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT &&
+      algo != GDN_ALGO_CHUNKED_COOP)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
   gdn_status st = check_heads(h_k, h_v, d_k, d_v);
@@ -166,7 +177,7 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
   if (qk_norm && algo == GDN_ALGO_CHUNKED_FUSED) return GDN_ERR_INVALID_ARG;
   const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
   const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
-                          algo == GDN_ALGO_CHUNKED_SPLIT;
+                          algo == GDN_ALGO_CHUNKED_SPLIT || algo == GDN_ALGO_CHUNKED_COOP;
   if (chunk_only && !chunk_ok)
     return dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE;
 
@@ -197,8 +208,19 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
   // The chunked evaluation runs as one fused kernel, or as two kernels meeting
   // in the caller's workspace (forced by GDN_ALGO_CHUNKED_SPLIT; otherwise when
   // the sequences are long enough and the workspace is large enough).
-  bool split = false;
-  if (run_chunk && algo != GDN_ALGO_CHUNKED_FUSED) {
+  bool split = false, coop = false;
+  if (run_chunk && algo == GDN_ALGO_CHUNKED_COOP) {
+    if (!workspace) return GDN_ERR_NULL_POINTER;
+    if (!aligned16(workspace)) return GDN_ERR_MISALIGNED;
+    if (workspace_bytes < gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v))
+      return GDN_ERR_WORKSPACE_TOO_SMALL;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    if (!gdn::coop_supported(num_seqs, h_v, d_v, sms)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    coop = true;
+  } else if (run_chunk && algo != GDN_ALGO_CHUNKED_FUSED) {
     const size_t need = gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
     if (algo == GDN_ALGO_CHUNKED_SPLIT) {
       if (!workspace) return GDN_ERR_NULL_POINTER;
@@ -214,12 +236,25 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
       a.min_chunk_len = INT32_MAX;
     }
   }
+  if (split && algo != GDN_ALGO_CHUNKED_SPLIT && total_tokens >= kCoopMinAvgTokens * num_seqs &&
+      workspace_bytes >= gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v)) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        gdn::coop_supported(num_seqs, h_v, d_v, sms)) {
+      coop = true;
+      split = false;
+    }
+  }
   st = error_word(&a.err);
   if (st != GDN_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (run_chunk) {
-    const cudaError_t e = split ? gdn::launch_chunked_split(a, workspace, s) : gdn::launch_chunked(a, s);
+    const cudaError_t e = coop    ? gdn::launch_chunked_coop(a, workspace, s)
+                          : split ? gdn::launch_chunked_split(a, workspace, s)
+                                  : gdn::launch_chunked(a, s);
+    if (e == cudaErrorNotSupported) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (e != cudaSuccess) return GDN_ERR_CUDA;
   }
   if (run_scan && gdn::launch_scan(a, s) != cudaSuccess) return GDN_ERR_CUDA;

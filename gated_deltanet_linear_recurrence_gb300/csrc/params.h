@@ -110,5 +110,12 @@ bool chunked_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dt
 // Two-kernel chunked prefill (prepare + chain) through a caller workspace.
 size_t split_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v);
 cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream);
+// One cooperative kernel (prepare slots and 64-row chains in one resident grid,
+// chained by per-item ready flags) through a caller workspace: the two-kernel
+// workspace plus one int per item.  Supported when d_v is a multiple of 64 and
+// the chains take at most two thirds of the SMs.
+size_t coop_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v);
+bool coop_supported(int32_t num_seqs, int32_t h_v, int32_t d_v, int sm_count);
+cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStream_t stream);
 
 }  // namespace gdn

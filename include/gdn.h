@@ -91,7 +91,10 @@ typedef enum {
   GDN_ALGO_CHUNKED = 2,       /* chunks of 64 tokens on tcgen05 tensor cores (bf16); the library
                                  picks the fused or the two-kernel form (see gdn_prefill) */
   GDN_ALGO_CHUNKED_FUSED = 3, /* chunked, one fused kernel, no workspace */
-  GDN_ALGO_CHUNKED_SPLIT = 4  /* chunked, two kernels through the workspace (required) */
+  GDN_ALGO_CHUNKED_SPLIT = 4, /* chunked, two kernels through the workspace (required) */
+  GDN_ALGO_CHUNKED_COOP = 5   /* chunked, one cooperative kernel through the workspace (required;
+                                 d_v a multiple of 64, num_seqs x h_v x d_v / 64 at most two
+                                 thirds of the SMs, else GDN_ERR_UNSUPPORTED_SHAPE) */
 } gdn_algo;
 
 /*
@@ -117,7 +120,12 @@ typedef enum {
  * they measured faster on GB300) and workspace_bytes is at least
  * gdn_prefill_workspace_size(...), else the fused kernel;
  * GDN_ALGO_CHUNKED_SPLIT always takes them and returns GDN_ERR_NULL_POINTER or
- * GDN_ERR_WORKSPACE_TOO_SMALL without one.  Results agree within rounding; the
+ * GDN_ERR_WORKSPACE_TOO_SMALL without one.  The same work also runs as one
+ * cooperative kernel whose prepare CTAs and state-pass CTAs overlap
+ * (GDN_ALGO_CHUNKED_COOP; AUTO and CHUNKED take it when the sequences average at
+ * least 8,192 tokens, its state passes fit and the workspace holds its ready
+ * flags; its results equal the two kernels' bit for bit).  Results agree
+ * within rounding; the
  * workspace is not used after the launches complete.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
@@ -142,9 +150,11 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
                           uint32_t options, gdn_stream_t stream);
 
 /* Bytes of workspace for the fastest gdn_prefill path with these arguments
- * (0 when that path uses none); for GDN_ALGO_CHUNKED_SPLIT, the bytes it
- * needs.  An upper bound computed from the host arguments: the 1 KB-rounded
- * (N+1) int32 header + (T/64 + N + 1) * h_v * 41 KB. */
+ * (0 when that path uses none); for GDN_ALGO_CHUNKED_SPLIT and
+ * GDN_ALGO_CHUNKED_COOP, the bytes each needs.  An upper bound computed from the
+ * host arguments: the 1 KB-rounded (N+1) int32 header + I * 41 KB with
+ * I = (T/64 + N + 1) * h_v items, plus (I + 1) int32 ready flags (1 KB-rounded)
+ * except for GDN_ALGO_CHUNKED_SPLIT. */
 size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
                                   int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                                   gdn_algo algo);

@@ -123,12 +123,16 @@ def test_workspace_and_crossover_queries(lib):
     assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 1) == 0  # scan needs none
     ws = lambda n, t, algo: lib.gdn_prefill_workspace_size(n, t, 16, 32, 128, 128, 1, algo)
     assert ws(1, 4096, 3) == 0                           # fused chunked kernel: none
-    assert ws(1, 4096, 2) == ws(1, 4096, 4) > 0          # long sequences: two kernels
+    # long sequences: two kernels, or the cooperative form (the same plus its flags)
+    assert ws(1, 4096, 2) == ws(1, 4096, 5) > ws(1, 4096, 4) > 0
     assert ws(4, 1000, 2) == 0 and ws(4, 1000, 0) == 0   # averaging 250 tokens: fused
     assert ws(4, 1000, 4) > 0                            # unless the two kernels are forced
-    assert ws(4, 2048, 2) == ws(4, 2048, 4) > 0
-    # header (1 KB-rounded) + (T/64 + N + 1) per-chunk packages of 41 KB per value head
-    assert ws(4, 2048, 4) == 1024 + (2048 // 64 + 5) * 32 * 41984
+    assert ws(4, 2048, 2) == ws(4, 2048, 5) > ws(4, 2048, 4) > 0
+    # header (1 KB-rounded) + I = (T/64 + N + 1) x h_v per-chunk packages of 41 KB
+    items = (2048 // 64 + 5) * 32
+    assert ws(4, 2048, 4) == 1024 + items * 41984
+    # the cooperative form adds one ready flag per item and a counter, 1 KB-rounded
+    assert ws(4, 2048, 5) == ws(4, 2048, 4) + ((items + 1) * 4 + 1023) // 1024 * 1024
     x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
     assert x > 0
     assert lib.gdn_prefill_crossover_tokens(16, 32, 128, 48, 1) == 2**31 - 1
