@@ -19,7 +19,7 @@
 //
 // chunk_chain_kernel walks each (sequence, value head, 32-row slice of d_v) in
 // chunk order with the fp32 state in TMEM, bulk-copying the packages into a
-// 3-stage ring next to the TMA'd Q, K and V slice:
+// 3-stage ring next to the TMA'd Q and K:
 //   D = [-W; Q] S^T,  U = U~ + D_top,
 //   S^T <- Gamma_n S^T + K^T (decay U),  O = Gamma D_bottom + P U.
 // Warp roles: a producer warp (copies), an MMA warp (one thread issues every
@@ -35,6 +35,11 @@
 // Compared with the single fused kernel (chunk_prefill.cu) the key-side work is
 // done once per head instead of once per slice, and the chain's SM no longer
 // shares its tensor pipe and shared memory with it.
+//
+// chunk_coop_kernel runs the same two parts in one cooperative grid, every CTA
+// resident: prepare slots publish a ready flag per package and the state passes
+// (64 rows of a head per CTA) follow them chunk by chunk, so the two overlap
+// instead of running one after the other; it pays off on long prompts.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
