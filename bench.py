@@ -36,35 +36,46 @@ FP32_LANES_PER_SM = 128
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of each kernel (summaries under profiles/), valid only while the
-# kernel's device sources (the .cu and the device headers it includes) hash to
-# the recorded value.
+# kernel's device sources (the .cu and the device headers it includes, comments
+# stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "8c6c1d8e790cc58d",
+                    "sha256_16": "306b5b4f8c58f83c",
                     "bytes": 6_144 + (68_259_072 + 29_017_600) + (118_790_912 + 12_413_440),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
     "attn_decode": {"files": ["attn_decode.cu", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "b85689230fdf4243", "bytes": 268_529_664 + 3_432_192,
+                    "sha256_16": "2377dfb50b6a2af5", "bytes": 268_529_664 + 3_432_192,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
-                    "sha256_16": "aeafdf16e54526c5", "bytes": 541_154_304 + 479_891_712,
+                    "sha256_16": "620ed98dc0429f3d", "bytes": 541_154_304 + 479_891_712,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
 
+def source_hash(files):
+    """Hash of the kernel sources with comments and blank lines removed, so that
+    documentation edits do not invalidate a capture but any code change does."""
+    import hashlib
+    import re
+
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_recurrence_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            line = line.split("//", 1)[0].rstrip()
+            if line:
+                m.update(line.encode() + b"\n")
+    return m.hexdigest()[:16]
+
+
 def ncu_traffic(kernel):
     """Recorded DRAM bytes per launch, or None if the kernel changed since the capture."""
-    import hashlib
-
     rec = NCU_TRAFFIC[kernel]
-    m = hashlib.sha256()
-    for f in rec["files"]:
-        with open(os.path.join(ROOT, "gated_deltanet_linear_recurrence_gb300", "csrc", f), "rb") as fh:
-            m.update(fh.read())
-    return rec["bytes"] if m.hexdigest()[:16] == rec["sha256_16"] else None
+    return rec["bytes"] if source_hash(rec["files"]) == rec["sha256_16"] else None
 
 
 def make_flush(torch, dev, l2):
