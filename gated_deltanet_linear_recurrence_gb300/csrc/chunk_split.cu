@@ -85,7 +85,8 @@ struct SplitParams {
   float scale;
   int32_t min_len;
   int qk_norm;          // q and k divided by their L2 norm (+1e-6 under the root)
-  int32_t* chunk_base;  // [N+1] in the workspace header
+  int32_t* chunk_base;  // [N+1] in the workspace header (unused when single)
+  int single;           // one sequence: chunk c is item c * h_v + h, no plan kernel ran
   uint8_t* packages;    // items x kPkgBytes
   int64_t max_items;
   int* err;
@@ -179,6 +180,18 @@ constexpr uint32_t IDP_W = tc::idesc_bf16_f32(64, 128, false, true);
 // id * h_v + value head); false past the last chunk.
 __device__ __forceinline__ bool item_chunk(const SplitParams& p, int64_t item, int& n, int& c) {
   const int64_t cid = item / p.h_v;
+  if (p.single) {  // no chunk table: the sequence's range is checked here instead
+    int64_t t0, t1;
+    if (!seq_range(p, 0, t0, t1)) {
+      if (item == 0) raise_error(p.err, kErrBadCuSeqlens);
+      return false;
+    }
+    const int64_t L = t1 - t0;
+    if (L < p.min_len || cid >= (L + kC - 1) / kC) return false;
+    n = 0;
+    c = (int)cid;
+    return true;
+  }
   if (cid >= p.chunk_base[p.num_seqs]) return false;
   // the sequence owning chunk cid: last n with chunk_base[n] <= cid (skipping empty ones)
   int lo = 0, hi = p.num_seqs - 1;
@@ -599,7 +612,10 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   const int jrow = 32 * (warp & 3) + lane;  // its TMEM lane: row of S^T (key dim)
   const int hk = h / (p.h_v / p.h_k);
   int64_t t_beg, t_end;
-  if (!seq_range(p, n, t_beg, t_end)) return;  // reported by the plan kernel
+  if (!seq_range(p, n, t_beg, t_end)) {  // reported by the plan kernel, or here for one sequence
+    if (p.single && tid == 0) raise_error(p.err, kErrBadCuSeqlens);
+    return;
+  }
   const int64_t L = t_end - t_beg;
   if (L < p.min_len) return;  // the token scan owns this sequence
   const int nchunks = (int)((L + kC - 1) / kC);
@@ -646,7 +662,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   bool ok = true;
   wait_prerequisites();  // the packages and chunk table (set-up above overlapped the prepare)
-  const int64_t first_item = (int64_t)p.chunk_base[n] * p.h_v + h;
+  const int64_t first_item = p.single ? h : (int64_t)p.chunk_base[n] * p.h_v + h;
 
   if (warp == CF::kProducerWarp) {
     if (lane == 0) {
@@ -1066,6 +1082,7 @@ bool split_setup(const PrefillArgs& a, void* workspace, CUtensorMap& mq, CUtenso
   p.packages = static_cast<uint8_t*>(workspace) + split_header_bytes(a.num_seqs);
   p.max_items = (int64_t)split_max_items(a.num_seqs, a.total_tokens, a.h_v);
   p.err = a.err;
+  p.single = a.num_seqs == 1 ? 1 : 0;
   return true;
 }
 
@@ -1093,8 +1110,10 @@ cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStrea
   if (resident < 1) return cudaErrorNotSupported;
   int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
                                       split_workspace_bytes(a.num_seqs, a.total_tokens, a.h_v));
-  chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
-  e = cudaGetLastError();
+  if (!p.single) {  // one sequence needs no chunk table
+    chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess)
     e = cudaMemsetAsync(flags, 0, (size_t)(p.max_items + 1) * sizeof(int), stream);
   if (e != cudaSuccess) return e;
@@ -1127,8 +1146,11 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
     return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (!p.single) {  // one sequence needs no chunk table
+    chunk_plan_kernel<<<1, 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
   // prepare and chain launch with programmatic stream serialization: each may
   // start its set-up before the kernel before it has finished (the kernels
   // wait for that kernel's results with griddepcontrol.wait)

@@ -168,6 +168,21 @@ def test_bad_cu_seqlens_reported(algo):
     assert torch.all(st[1] == 5.0)
 
 
+@pytest.mark.parametrize("algo", ["chunked_split", "chunked_coop"])
+def test_bad_cu_seqlens_one_sequence(algo):
+    """One sequence (no chunk-table kernel: the kernels check the range
+    themselves) whose cu_seqlens ends past total_tokens: reported, and neither
+    the output nor the state is touched."""
+    d = inputs.make_prefill([130], 1, 2, 128, 64, "bf16", seed=17)
+    x = dev(d)
+    cu = torch.tensor([0, 200], dtype=torch.int32, device="cuda")
+    st = torch.full((1, 2, 64, 128), 5.0, device="cuda")
+    o = torch.zeros((130, 2, 64), dtype=torch.bfloat16, device="cuda")
+    gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, state_out=st, o=o, algo=algo)
+    assert gdn_stream_status() == "GDN_ERR_BAD_CU_SEQLENS"
+    assert torch.all(st == 5.0) and torch.count_nonzero(o.float()) == 0
+
+
 @pytest.fixture(scope="module")
 def long_prefill():
     w = inputs.WORKLOADS["prefill_t131072"]
