@@ -40,8 +40,8 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "306b5b4f8c58f83c",
-                    "bytes": 6_144 + (68_259_072 + 29_017_600) + (118_790_912 + 12_413_440),
+                    "sha256_16": "d2ebf6857aac4b2a",
+                    "bytes": (68_250_880 + 31_689_984) + (118_797_056 + 12_399_872),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
@@ -364,7 +364,10 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1e3)
     # chunked with workspace: plan + prepare + chain kernels; fused or scan: one kernel
-    launches_per_step = 3 if (algo_used.startswith("chunked") and ws_n > 0) else 1
+    # chunked with workspace: prepare + chain kernels, plus the chunk-table kernel for more
+    # than one sequence; fused or scan: one kernel
+    launches_per_step = ((2 if len(lengths) == 1 else 3)
+                         if (algo_used.startswith("chunked") and ws_n > 0) else 1)
 
     # roofline of the prefill kernel (one launch per step)
     if algo_used.startswith("chunked"):
@@ -374,8 +377,8 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                 "traffic": ncu_traffic("chunk_split" if split else "chunk_prefill"),
-                "scope": ("the whole gdn_prefill call: chunk_plan + chunk_prepare + chunk_chain "
-                          "kernels (one algorithm split in two; shares in profiles/)") if split
+                "scope": ("the whole gdn_prefill call: chunk_prepare + chunk_chain kernels (one "
+                          "algorithm split in two; shares in profiles/)") if split
                          else "the fused chunk_prefill kernel",
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
                 "algorithmic_flop_per_launch": flop}
