@@ -368,16 +368,21 @@ __global__ void __launch_bounds__(kAThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, kAttnTmemCols);
 }
 
-// Merge the fixed-block partials of one (sequence, query head), 256 threads:
-// o = sum_s e^{m_s - M} acc_s / sum_s e^{m_s - M} l_s with M = max_s m_s.  The
-// maximum and the weights are computed across the threads (one split each),
-// then each thread sums its dimension over the splits with independent loads.
-constexpr int kCombineThreads = kD;
+// Merge the fixed-block partials of one (sequence, query head):
+// o = sum_s e^{m_s - M} acc_s / sum_s e^{m_s - M} l_s with M = max_s m_s.  A block
+// takes 64 of the 256 dimensions with four groups of threads, each summing every
+// fourth split, so that many independent loads are in flight; the maximum, the
+// weights and the normaliser are computed across the block (one split per thread).
+constexpr int kCombineDims = 64, kCombineGroups = 4;
+constexpr int kCombineThreads = kCombineDims * kCombineGroups;
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const AttnArgs p) {
   tc::wait_prerequisites();  // the partials of the attention kernel
-  __shared__ float wsm[kCombineThreads], lsm[kCombineThreads], rsm[kCombineThreads / 32];
+  __shared__ float wsm[kCombineThreads], rsm[kCombineThreads / 32],
+      part[kCombineGroups][kCombineDims];
   const int64_t bh = blockIdx.x;
+  const int d0 = blockIdx.y * kCombineDims;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int dl = t % kCombineDims, grp = t / kCombineDims;
   const int64_t stride = kD + 2;
   const float* base = p.partial + bh * (int64_t)p.n_split * stride;
   float mx = -INFINITY;
@@ -389,6 +394,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Att
   float M = rsm[0];
 #pragma unroll
   for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, rsm[w]);
+  __syncthreads();  // rsm is reused for the normaliser below
   float num = 0.f, den = 0.f;
   for (int c0 = 0; c0 < p.n_split; c0 += kCombineThreads) {
     const int n = min(kCombineThreads, p.n_split - c0);
@@ -396,18 +402,28 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Att
       const float ms = base[(c0 + t) * stride + kD];
       const float w = (ms == -INFINITY || M == -INFINITY) ? 0.f : exp_f(ms - M);
       wsm[t] = w;
-      lsm[t] = w * base[(c0 + t) * stride + kD + 1];
+      den = fmaf(w, base[(c0 + t) * stride + kD + 1], den);
     }
     __syncthreads();
-    const float* col = base + (int64_t)c0 * stride + t;
+    const float* col = base + (int64_t)c0 * stride + d0 + dl;
 #pragma unroll 8
-    for (int j = 0; j < n; ++j) {
-      num = fmaf(wsm[j], col[j * stride], num);
-      den += lsm[j];
-    }
+    for (int j = grp; j < n; j += kCombineGroups) num = fmaf(wsm[j], col[j * stride], num);
     __syncthreads();
   }
-  static_cast<__nv_bfloat16*>(p.o)[bh * kD + t] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
+  if (lane == 0) rsm[warp] = den;
+  part[grp][dl] = num;
+  __syncthreads();
+  if (grp == 0) {
+    float tot = 0.f, l = 0.f;
+#pragma unroll
+    for (int g2 = 0; g2 < kCombineGroups; ++g2) tot += part[g2][dl];
+#pragma unroll
+    for (int w = 0; w < kCombineThreads / 32; ++w) l += rsm[w];
+    static_cast<__nv_bfloat16*>(p.o)[bh * kD + d0 + dl] =
+        __float2bfloat16_rn(l > 0.f ? tot / l : 0.f);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -501,7 +517,7 @@ cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t stream) {
   cfg.dynamicSmemBytes = kAttnSmem;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, mk, mv, a);
   if (e != cudaSuccess || a.n_split == 1) return e;
-  cfg.gridDim = dim3((unsigned)((int64_t)a.batch * a.h_q));
+  cfg.gridDim = dim3((unsigned)((int64_t)a.batch * a.h_q), kD / kCombineDims);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel, a);
