@@ -47,7 +47,7 @@ NCU_TRAFFIC = {
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
     "attn_decode": {"files": ["attn_decode.cu", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "2377dfb50b6a2af5", "bytes": 268_529_664 + 3_432_192,
+                    "sha256_16": "5f6befb361bfe092", "bytes": 268_506_368 + 2_978_048,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
                     "sha256_16": "620ed98dc0429f3d", "bytes": 541_154_304 + 479_891_712,

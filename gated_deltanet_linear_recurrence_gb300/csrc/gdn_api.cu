@@ -77,7 +77,7 @@ int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dt
 
 constexpr int32_t kAttnHeadDim = 256;
 constexpr int32_t kAttnMaxGroup = 8;
-constexpr int32_t kAttnMinBlock = 512;  // the smallest block the library picks
+constexpr int32_t kAttnMinBlock = 128;  // the smallest block the library picks
 
 gdn_status attn_shape(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim,
                       int32_t capacity, int layout, int32_t block_keys) {

@@ -357,7 +357,7 @@ gdn_status gdn_attn_decode(const void* q, const void* k_cache, const void* v_cac
 
 /* Workspace bytes sufficient for gdn_attn_decode with these arguments, computed
  * on the host: 0 for GDN_ATTN_GENERAL, else batch x h_q x n x (head_dim + 2) x
- * 4 with n = ceil(capacity / block_keys), block_keys taken as 512 when 0 (the
+ * 4 with n = ceil(capacity / block_keys), block_keys taken as 128 when 0 (the
  * smallest block the library picks).  0 for invalid arguments. */
 size_t gdn_attn_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
                                       int32_t head_dim, int32_t capacity,

@@ -219,11 +219,11 @@ def test_attn_decode_host_errors(lib):
 
 def test_attn_workspace_size(lib):
     """Workspace bound: 0 for the general layout, else B x h_q x n x (D + 2) x 4
-    with n = ceil(capacity / block), block 512 when the library picks it."""
+    with n = ceil(capacity / block), block 128 when the library picks it."""
     f = lib.gdn_attn_decode_workspace_size
     assert f(1, 16, 2, 256, 131072, 1, 0) == 0
     assert f(1, 16, 2, 256, 131072, 2, 2048) == 1 * 16 * 64 * 258 * 4
-    assert f(3, 16, 2, 256, 131072, 0, 0) == 3 * 16 * 256 * 258 * 4
+    assert f(3, 16, 2, 256, 131072, 0, 0) == 3 * 16 * 1024 * 258 * 4
     assert f(2, 8, 1, 256, 1000, 2, 512) == 2 * 8 * 2 * 258 * 4
     assert f(2, 8, 1, 256, 512, 2, 512) == 0              # a single block needs no merge
     assert f(1, 16, 2, 128, 4096, 0, 0) == 0              # invalid shape
