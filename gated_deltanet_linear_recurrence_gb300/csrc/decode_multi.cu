@@ -17,7 +17,6 @@
 
 #include "params.h"
 #include "rows.cuh"
-#include "tc.cuh"
 
 namespace gdn {
 namespace {
@@ -45,9 +44,6 @@ __global__ void __launch_bounds__(kMultiWarps * 32)
   const int lam = lane % L;
   const int hk = h / (h_v / h_k);
   const int64_t bh = (int64_t)b * h_v + h;
-  // programmatic stream serialization, as in the single-token step
-  tc::allow_dependents();
-  tc::wait_prerequisites();
   const int64_t row_off = (int64_t)(row0 + grp) * DK + 4 * lam;  // within one head's state
 
   float* srow = state + bh * d_v * (int64_t)DK + row_off;
@@ -115,19 +111,15 @@ cudaError_t launch_t(const DecodeMultiArgs& a, cudaStream_t stream) {
   const int blocks_per_head = (a.d_v + rows_per_block - 1) / rows_per_block;
   const int64_t gx = (int64_t)a.batch * blocks_per_head;
   if (gx > 0x7fffffffLL || a.h_v > 65535) return cudaErrorInvalidConfiguration;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)gx, (unsigned)a.h_v);
-  cfg.blockDim = dim3(kMultiWarps * 32);
-  cfg.stream = stream;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_multi_kernel<DK, R, T>, static_cast<const T*>(a.q),
-                            static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g, a.beta,
-                            a.state, static_cast<T*>(a.o), a.snapshots, a.n_tokens, a.h_k, a.h_v,
-                            a.d_v, blocks_per_head, a.scale, a.qk_norm);
+  // Plain launch: with programmatic stream serialization (as the single-token
+  // step uses) back-to-back calls measured 6 % slower (212 vs 199 us at 256
+  // sequences x 4 tokens), the next grid's early CTAs competing with this one's.
+  dim3 grid((unsigned)gx, (unsigned)a.h_v);
+  decode_multi_kernel<DK, R, T><<<grid, kMultiWarps * 32, 0, stream>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g,
+      a.beta, a.state, static_cast<T*>(a.o), a.snapshots, a.n_tokens, a.h_k, a.h_v, a.d_v,
+      blocks_per_head, a.scale, a.qk_norm);
+  return cudaGetLastError();
 }
 
 // The decode step's choice of rows per lane group (same rows, same reduction
