@@ -65,3 +65,34 @@ def test_library_choice_takes_the_cooperative_form():
         outs.append((o, s))
     for o, s in outs[1:]:
         assert torch.equal(outs[0][0], o) and torch.equal(outs[0][1], s)
+
+
+def test_auto_mixes_the_cooperative_form_and_the_scan():
+    """AUTO on a batch averaging more than 8,192 tokens with one sequence below the
+    scan crossover: the long sequence runs the cooperative form, the short one the
+    token scan, in the same call; both against the fp64 oracle."""
+    import numpy as np
+    import oracle
+
+    x = inputs.make_prefill([16500, 9], 2, 4, 128, 64, "bf16", seed=21, state_std=0.02)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    o, s = gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                       state_in=d["state_in"], algo="auto")
+    torch.cuda.synchronize()
+    assert gdn_stream_status() == "GDN_OK"
+    o_ref, s_ref = oracle.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                                  2, 4, 128, 64, state_in=x["state_in"])
+
+    def rel(a, b):
+        a = np.asarray(a, np.float64)
+        return float(np.linalg.norm((a - b).ravel()) / np.linalg.norm(b.ravel()))
+
+    assert rel(o.float().cpu().numpy(), o_ref) < 8e-3
+    assert rel(s.cpu().numpy(), s_ref) < 8e-3
+    # the short sequence alone through the scan: bitwise the same rows
+    t0 = 16500
+    o9, s9 = gdn_prefill(d["q"][t0:], d["k"][t0:], d["v"][t0:], d["g"][t0:], d["beta"][t0:],
+                         torch.tensor([0, 9], dtype=torch.int32, device="cuda"),
+                         state_in=d["state_in"][1:].contiguous(), algo="scan")
+    torch.cuda.synchronize()
+    assert torch.equal(o9, o[t0:]) and torch.equal(s9[0], s[1])
