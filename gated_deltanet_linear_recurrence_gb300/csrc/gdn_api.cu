@@ -251,10 +251,18 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (run_chunk) {
-    const cudaError_t e = coop    ? gdn::launch_chunked_coop(a, workspace, s)
-                          : split ? gdn::launch_chunked_split(a, workspace, s)
-                                  : gdn::launch_chunked(a, s);
-    if (e == cudaErrorNotSupported) return GDN_ERR_UNSUPPORTED_SHAPE;
+    cudaError_t e = coop    ? gdn::launch_chunked_coop(a, workspace, s)
+                    : split ? gdn::launch_chunked_split(a, workspace, s)
+                            : gdn::launch_chunked(a, s);
+    // The cooperative grid needs every SM free for it; when AUTO or CHUNKED chose
+    // it and the launch is refused (other work holds SMs), the two kernels run.
+    if (coop && algo != GDN_ALGO_CHUNKED_COOP &&
+        (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge)) {
+      (void)cudaGetLastError();  // a refused launch configuration, not a sticky error
+      e = gdn::launch_chunked_split(a, workspace, s);
+    }
+    if (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge)
+      return GDN_ERR_UNSUPPORTED_SHAPE;
     if (e != cudaSuccess) return GDN_ERR_CUDA;
   }
   if (run_scan && gdn::launch_scan(a, s) != cudaSuccess) return GDN_ERR_CUDA;
