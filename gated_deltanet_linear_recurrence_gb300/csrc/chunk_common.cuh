@@ -92,8 +92,9 @@ __device__ __forceinline__ void store_16x8(float* C, int ldc, const float (&c)[4
 // as [[T0, 0], [-T1 A10 T0, T1]], then the 64x64 matrix the same way; the block
 // products of the last two levels run on the warp tensor cores in tf32.  Each
 // level only overwrites blocks that later levels read as T.
-template <uint32_t kBar, uint32_t kCount>
-__device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt, int lane) {
+template <uint32_t kCount>
+__device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt, int lane,
+                                                   uint32_t bar) {
   const int pw = pt >> 5;
   if (pw < 2) {  // level 1: warp pw handles diagonal blocks 2pw, 2pw+1; lane = column
     const int blk = 2 * pw + (lane >> 4), cc = lane & 15, o = 16 * blk;
@@ -119,7 +120,7 @@ __device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt,
 #pragma unroll
     for (int r = 0; r < 16; ++r) MF[(o + r) * kLdM + o + cc] = x[r];
   }
-  tc::named_sync(kBar, kCount);
+  tc::named_sync(bar, kCount);
   // level 2: pairs (0,1) and (2,3): Y = A10 T0 (warps 0-3: pair, 8-column tile)
   if (pw < 4) {
     const int pr = pw >> 1, nt = pw & 1, o0 = 32 * pr, o1 = o0 + 16;
@@ -127,14 +128,14 @@ __device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt,
     warp_mma_16x8<16>(c, MF + o1 * kLdM + o0, kLdM, MF + o0 * kLdM + o0 + 8 * nt, kLdM, lane);
     store_16x8(YF + (16 * pr) * kLdY + 8 * nt, kLdY, c, 1.f, lane);
   }
-  tc::named_sync(kBar, kCount);
+  tc::named_sync(bar, kCount);
   if (pw < 4) {  // T10 = -T1 Y
     const int pr = pw >> 1, nt = pw & 1, o0 = 32 * pr, o1 = o0 + 16;
     float c[4];
     warp_mma_16x8<16>(c, MF + o1 * kLdM + o1, kLdM, YF + (16 * pr) * kLdY + 8 * nt, kLdY, lane);
     store_16x8(MF + o1 * kLdM + o0 + 8 * nt, kLdM, c, -1.f, lane);
   }
-  tc::named_sync(kBar, kCount);
+  tc::named_sync(bar, kCount);
   // level 3, eight 16x8 tiles (rows 16 (tile >> 2), columns 8 (tile & 3)) over the warps
   constexpr int kWarps = (int)(kCount / 32);
   static_assert(kWarps >= 4 && 8 % kWarps == 0, "the solve runs on 4 or 8 warps");
@@ -144,14 +145,14 @@ __device__ __forceinline__ void unit_lower_inverse(float* MF, float* YF, int pt,
     warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM, kLdM, MF + 8 * nt, kLdM, lane);
     store_16x8(YF + (16 * mt) * kLdY + 8 * nt, kLdY, c, 1.f, lane);
   }
-  tc::named_sync(kBar, kCount);
+  tc::named_sync(bar, kCount);
   for (int tile = pw; tile < 8; tile += kWarps) {  // T_BL = -T_BR Y
     const int mt = tile >> 2, nt = tile & 3;
     float c[4];
     warp_mma_16x8<32>(c, MF + (32 + 16 * mt) * kLdM + 32, kLdM, YF + 8 * nt, kLdY, lane);
     store_16x8(MF + (32 + 16 * mt) * kLdM + 8 * nt, kLdM, c, -1.f, lane);
   }
-  tc::named_sync(kBar, kCount);
+  tc::named_sync(bar, kCount);
 }
 
 

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       group_sync(kBarPrep, kPrepThreads);
 
-      unit_lower_inverse<kBarPrep, kPrepThreads>(MF, YF, pt, lane);
+      unit_lower_inverse<kPrepThreads>(MF, YF, pt, lane, kBarPrep);
 
       {  // operands T diag(b Gamma) and T diag(b): thread = (row r, 16-column quarter)
         const int r = pt >> 2, q = pt & 3;

@@ -223,13 +223,15 @@ __device__ __forceinline__ void prepare_loads(const SplitParams& p, const CUtens
 // One prepare item (chunk, value head) on 128 threads (pt = 0..127) with the
 // shared-memory layout above at `smem`, 128 TMEM columns at `tmem`, three
 // mbarriers `bars` (Q/K landed, an MMA done, V landed; initialised with count 1)
-// that have seen k earlier items, and the named barriers kBA (128 threads) and
-// kBG (threads 0-63); prepare_loads has been issued for it.  Writes the item's
+// that have seen k earlier items, and the named barriers bA (128 threads) and
+// bG (threads 0-63); prepare_loads has been issued for it.  Writes the item's
 // package; false if a wait expired.
-template <uint32_t kBA, uint32_t kBG>
+// The barrier ids are run-time values so that the cooperative form's four
+// slots run one copy of this code (instruction-cache footprint).
 __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtensorMap* tm_v,
                                              uint8_t* smem, uint32_t tmem, uint64_t* bars,
-                                             uint32_t k, int pt, int64_t item, int n, int c) {
+                                             uint32_t k, int pt, int64_t item, int n, int c,
+                                             uint32_t bA, uint32_t bG) {
   const int pw = pt >> 5, lane = pt & 31;
   const int h = (int)(item % p.h_v);
   const int64_t t_beg = p.cu[n], t_end = p.cu[n + 1];
@@ -253,7 +255,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
   const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
   bool ok = tc::mbar_wait(bar_tma, k & 1);
   tc::fence_after_sync();
-  ok = tc::named_sync_and(kBA, kPrepThreads, ok);
+  ok = tc::named_sync_and(bA, kPrepThreads, ok);
   if (ok) {
     if (pt == 64) {  // G = [Q;K] K^T: rows 0-63 Q K^T, rows 64-127 K K^T
 #pragma unroll
@@ -297,7 +299,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
         if (lane >= off) x += yv;
       }
       if (pt == 31) MF[0] = x;
-      tc::named_sync(kBG, 64);
+      tc::named_sync(bG, 64);
       if (pw == 1) x += MF[0];
       gam[pt] = x;
       const float Gx = tc::fast_exp(x);
@@ -313,7 +315,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
         MF[2 + pw] = lo;
         MF[4 + pw] = hi;
       }
-      tc::named_sync(kBG, 64);
+      tc::named_sync(bG, 64);
       dec[pt] = tc::fast_exp(gam[kC - 1] - x);
       // exp(gamma_r - gamma_i) = Gamma_r / Gamma_i without overflow or underflow
       // while every gamma of the chunk lies in [-kFactorRange, kFactorRange]
@@ -323,7 +325,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     }
     ok = tc::mbar_wait(bar_mma, (3 * k) & 1);
     tc::fence_after_sync();
-    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
+    ok = tc::named_sync_and(bA, kPrepThreads, ok);
     if (pt < 64) {  // the chain's per-row factors: Gamma_r / |q_r| for the output, decay_r / |k_r|
       float* gout = reinterpret_cast<float*>(pkg + kPkgGates);
       gout[pt] = Gam[pt] * rq[pt];
@@ -391,10 +393,10 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
       }
     }
     tc::fence_before_sync();
-    tc::named_sync(kBA, kPrepThreads);
+    tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
 
-    unit_lower_inverse<kBA, kPrepThreads>(MF, YF, pt, lane);
+    unit_lower_inverse<kPrepThreads>(MF, YF, pt, lane, bA);
 
     {  // T diag(b Gamma) over Q1 (W operand), T diag(b) over the start of MF (U~ operand)
       const int rr = pt >> 1, q = pt & 1;  // row rr, columns 32 q .. 32 q + 31
@@ -404,7 +406,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
         const float4 m = *reinterpret_cast<const float4*>(MF + rr * kLdM + 32 * q + 4 * e4);
         t[4 * e4] = m.x; t[4 * e4 + 1] = m.y; t[4 * e4 + 2] = m.z; t[4 * e4 + 3] = m.w;
       }
-      tc::named_sync(kBA, kPrepThreads);  // every row of T is read before TA overwrites MF
+      tc::named_sync(bA, kPrepThreads);  // every row of T is read before TA overwrites MF
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         const int ii = 32 * q + 8 * c8;
@@ -420,7 +422,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    tc::named_sync(kBA, kPrepThreads);
+    tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
     if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
 #pragma unroll
@@ -432,7 +434,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     }
     ok = tc::mbar_wait(bar_mma, (3 * k + 1) & 1);
     tc::fence_after_sync();
-    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
+    ok = tc::named_sync_and(bA, kPrepThreads, ok);
   }
   if (ok) {
     if (pt == 0) {  // K is consumed: V (two 64-column boxes) over K0 and K1
@@ -460,7 +462,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
       }
     }
     tc::fence_before_sync();
-    tc::named_sync(kBA, kPrepThreads);  // W's columns are read before U~ overwrites them
+    tc::named_sync(bA, kPrepThreads);  // W's columns are read before U~ overwrites them
     tc::fence_after_sync();
     if (pt == 64 && tc::mbar_wait(bar_v, k & 1)) {  // (on a timeout nothing commits: all time out)
       tc::fence_after_sync();
@@ -473,7 +475,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     }
     ok = tc::mbar_wait(bar_mma, (3 * k + 2) & 1);
     tc::fence_after_sync();
-    ok = tc::named_sync_and(kBA, kPrepThreads, ok);
+    ok = tc::named_sync_and(bA, kPrepThreads, ok);
     if (ok) {  // U~ slices (bf16, 64-byte rows with the SW64 XOR pattern) to the package
 #pragma unroll 1
       for (int sl = 0; sl < 4; ++sl) {
@@ -518,8 +520,8 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const bool ok = prepare_item<kBarAll, kBarGateP>(p, &tm_v, smem, *tmem_slot, bars,
-                                                   0, pt, item, n, c);
+  const bool ok = prepare_item(p, &tm_v, smem, *tmem_slot, bars, 0, pt, item, n, c, kBarAll,
+                               kBarGateP);
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
   __syncthreads();
@@ -956,12 +958,12 @@ static_assert(kCoopSmem <= 227 * 1024, "shared memory budget");
 static_assert(kCoopSlots * kPrepTmemCols <= 512, "TMEM of the prepare slots");
 
 // One prepare slot: 128 threads with their own shared memory, TMEM, mbarriers
-// and named barriers kBA, kBG, taking items from a counter shared by all slots
+// and named barriers bA, bG, taking items from a counter shared by all slots
 // (flags[max_items], zero at launch) in increasing order, i.e. chunk by chunk.
-template <uint32_t kBA, uint32_t kBG>
 __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CUtensorMap* tm_q,
                                                   const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                                  uint8_t* smem, int pt, int* flags) {
+                                                  uint8_t* smem, int pt, int* flags, uint32_t bA,
+                                                  uint32_t bG) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PP_MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
   int* next = reinterpret_cast<int*>(bars + 4);  // the slot's item, from the shared counter
@@ -971,33 +973,33 @@ __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CU
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
-  tc::named_sync(kBA, kPrepThreads);
+  tc::named_sync(bA, kPrepThreads);
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
   uint32_t k = 0;
   for (;; ++k) {
     if (pt == 0) *next = atomicAdd(flags + p.max_items, 1);
-    tc::named_sync(kBA, kPrepThreads);
+    tc::named_sync(bA, kPrepThreads);
     const int64_t item = *next;
     int n, c;
     if (!ok || item >= p.max_items || !item_chunk(p, item, n, c)) break;  // past the last chunk
     if (pt == 0) prepare_loads(p, tm_q, tm_k, smem, bars, item, n, c);
-    ok = prepare_item<kBA, kBG>(p, tm_v, smem, tmem, bars, k, pt, item, n, c);
+    ok = prepare_item(p, tm_v, smem, tmem, bars, k, pt, item, n, c, bA, bG);
     // Every thread's package stores are visible device-wide before the flag;
     // the slot's shared memory and TMEM are free for the next item.
     __threadfence();
     asm volatile("fence.proxy.async.global;" ::: "memory");
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    tc::named_sync(kBA, kPrepThreads);
+    tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
     if (pt == 0 && ok)
       asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flags + item), "r"(1) : "memory");
   }
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
-  tc::named_sync(kBA, kPrepThreads);
+  tc::named_sync(bA, kPrepThreads);
   tc::fence_after_sync();
   if (pt < 32) tc::tmem_dealloc(tmem, kPrepTmemCols);
 }
@@ -1024,12 +1026,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
   wait_prerequisites();  // the chunk table of the plan kernel
   const int slot = threadIdx.x / kPrepThreads, pt = threadIdx.x % kPrepThreads;
   uint8_t* sm = smem + slot * kPrepSlotBytes;
-  switch (slot) {
-    case 0: coop_prepare_slot<1, 2>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
-    case 1: coop_prepare_slot<3, 4>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
-    case 2: coop_prepare_slot<5, 6>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
-    default: coop_prepare_slot<7, 8>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags); break;
-  }
+  // named barriers 1 + 2 slot (the slot's 128 threads) and 2 + 2 slot (its first 64)
+  coop_prepare_slot(p, &tm_q, &tm_k, &tm_v, sm, pt, flags, 1u + 2u * slot, 2u + 2u * slot);
 }
 
 }  // namespace
