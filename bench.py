@@ -40,9 +40,12 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "d2ebf6857aac4b2a",
-                    "bytes": (68_250_880 + 31_689_984) + (118_797_056 + 12_399_872),
+                    "sha256_16": "2d02727ca58fd2d4",
+                    "bytes": (68_260_608 + 31_671_808) + (118_790_400 + 12_266_240),
                     "profile": "profiles/chunk_split_t4096.md"},
+    "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
+                   "sha256_16": "2d02727ca58fd2d4", "bytes": 68_684_288 + 67_595_264,
+                   "profile": "profiles/chunk_coop_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
@@ -296,7 +299,7 @@ def main():
     import torch
     import torch.distributed as dist
     from gated_deltanet_linear_recurrence_gb300 import (_lib, gdn_decode_step, gdn_prefill,
-                                                        gdn_prefill_crossover_tokens,
+                                                        gdn_prefill_form,
                                                         gdn_prefill_workspace_size,
                                                         gdn_stream_status, inputs)
     from gated_deltanet_linear_recurrence_gb300.shard import seq_shard
@@ -326,8 +329,10 @@ def main():
     ws_n = gdn_prefill_workspace_size(1, T, h_k, h_v, d_k, d_v, torch.bfloat16, args.algo)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cross = gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, torch.bfloat16)
-    algo_used = args.algo if args.algo != "auto" else ("chunked" if T >= cross else "scan")
+    # the evaluation the call runs (the library's own routing, queried)
+    form = gdn_prefill_form(len(lengths), T, h_k, h_v, d_k, d_v, torch.bfloat16, args.algo,
+                            ws_n)
+    algo_used = form
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = make_flush(torch, dev, l2)
@@ -363,23 +368,24 @@ def main():
         total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1e3)
-    # chunked with workspace: plan + prepare + chain kernels; fused or scan: one kernel
-    # chunked with workspace: prepare + chain kernels, plus the chunk-table kernel for more
-    # than one sequence; fused or scan: one kernel
-    launches_per_step = ((2 if len(lengths) == 1 else 3)
-                         if (algo_used.startswith("chunked") and ws_n > 0) else 1)
+    # two kernels: prepare + chain; cooperative: one kernel; either plus the chunk-table
+    # kernel for more than one sequence; fused or scan: one kernel
+    multi = 1 if len(lengths) > 1 else 0
+    launches_per_step = {"chunked_split": 2 + multi, "chunked_coop": 1 + multi}.get(form, 1)
 
     # roofline of the prefill kernel (one launch per step)
     if algo_used.startswith("chunked"):
         flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
-        split = ws_n > 0
+        scope, traffic_key = {
+            "chunked_coop": ("the whole gdn_prefill call: one cooperative kernel, prepare slots "
+                             "and state passes overlapped (profiles/)", "chunk_coop"),
+            "chunked_split": ("the whole gdn_prefill call: chunk_prepare + chunk_chain kernels "
+                              "(one algorithm split in two; shares in profiles/)", "chunk_split"),
+        }.get(form, ("the fused chunk_prefill kernel", "chunk_prefill"))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": ncu_traffic("chunk_split" if split else "chunk_prefill"),
-                "scope": ("the whole gdn_prefill call: chunk_prepare + chunk_chain kernels (one "
-                          "algorithm split in two; shares in profiles/)") if split
-                         else "the fused chunk_prefill kernel",
+                "traffic": ncu_traffic(traffic_key), "scope": scope,
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
                 "algorithmic_flop_per_launch": flop}
     else:

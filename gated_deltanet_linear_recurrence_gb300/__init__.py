@@ -17,7 +17,8 @@ __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspac
            "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi", "gdn_attn_decode",
            "gdn_attn_decode_workspace_size", "gdn_attn_decode_block_keys",
            "gdn_prefill_workspace_size",
-           "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens", "GdnError",
+           "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens",
+           "gdn_prefill_form", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
 NOALLOC_SCRATCH_BYTES = 96 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
@@ -52,6 +53,19 @@ def gdn_status_string(status):
 
 def gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, dtype=torch.bfloat16):
     return int(_lib.load().gdn_prefill_crossover_tokens(h_k, h_v, d_k, d_v, _DTYPES[dtype]))
+
+
+def gdn_prefill_form(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype=torch.bfloat16,
+                     algo="auto", workspace_bytes=0, qk_l2norm=False, sm_count=0):
+    """Name of the evaluation gdn_prefill would run for these sizes ("scan",
+    "chunked_fused", "chunked_split" or "chunked_coop"; see gdn_prefill_form in
+    include/gdn.h).  Raises GdnError for arguments the call would refuse."""
+    r = int(_lib.load().gdn_prefill_form(num_seqs, total_tokens, h_k, h_v, d_k, d_v,
+                                         _DTYPES[dtype], _lib.ALGOS[algo], int(workspace_bytes),
+                                         _options(qk_l2norm), int(sm_count)))
+    if r < 0:
+        raise GdnError(-r, "gdn_prefill_form")
+    return {v: k for k, v in _lib.ALGOS.items()}[r]
 
 
 def gdn_prefill_workspace_size(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype=torch.bfloat16,

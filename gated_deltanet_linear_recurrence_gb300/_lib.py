@@ -59,6 +59,8 @@ SIGNATURES = {
     "gdn_stream_status": (ctypes.c_int, [_vp]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_prefill_crossover_tokens": (_i32, [_i32, _i32, _i32, _i32, ctypes.c_int]),
+    "gdn_prefill_form": (_i32, [_i32, _i64, _i32, _i32, _i32, _i32, ctypes.c_int, ctypes.c_int,
+                                _sz, ctypes.c_uint32, _i32]),
 }
 
 _LIB = None

@@ -957,13 +957,20 @@ static_assert(CoopChain::kThreads <= kCoopThreads, "the chain fits in the grid's
 static_assert(kCoopSmem <= 227 * 1024, "shared memory budget");
 static_assert(kCoopSlots * kPrepTmemCols <= 512, "TMEM of the prepare slots");
 
+// Slot s of a CTA starts kSlotStaggerNs x s after slot 0: the first items
+// (the first chunks, which every state pass waits for) then do not all pass
+// through the same phases on an SM at once.
+constexpr uint32_t kSlotStaggerNs = 2000;
+
 // One prepare slot: 128 threads with their own shared memory, TMEM, mbarriers
-// and named barriers bA, bG, taking items from a counter shared by all slots
-// (flags[max_items], zero at launch) in increasing order, i.e. chunk by chunk.
+// and named barriers bA, bG.  Its first item is `first` (slot s of prepare CTA
+// r takes s x n_prep + r, so the first chunks spread over the SMs); later items
+// come from a counter shared by all n_slots slots (flags[max_items], zero at
+// launch), in increasing order, i.e. chunk by chunk.
 __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CUtensorMap* tm_q,
                                                   const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                   uint8_t* smem, int pt, int* flags, uint32_t bA,
-                                                  uint32_t bG) {
+                                                  uint32_t bG, int slot, int first, int n_slots) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PP_MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
   int* next = reinterpret_cast<int*>(bars + 4);  // the slot's item, from the shared counter
@@ -976,10 +983,14 @@ __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CU
   tc::named_sync(bA, kPrepThreads);
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (pt == 0 && slot > 0) {  // a fixed delay (a sleep, not a wait on anything)
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (tc::globaltimer_ns() - t0 < (uint64_t)slot * kSlotStaggerNs) __nanosleep(256);
+  }
   bool ok = true;
   uint32_t k = 0;
   for (;; ++k) {
-    if (pt == 0) *next = atomicAdd(flags + p.max_items, 1);
+    if (pt == 0) *next = k == 0 ? first : n_slots + atomicAdd(flags + p.max_items, 1);
     tc::named_sync(bA, kPrepThreads);
     const int64_t item = *next;
     int n, c;
@@ -1027,7 +1038,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
   const int slot = threadIdx.x / kPrepThreads, pt = threadIdx.x % kPrepThreads;
   uint8_t* sm = smem + slot * kPrepSlotBytes;
   // named barriers 1 + 2 slot (the slot's 128 threads) and 2 + 2 slot (its first 64)
-  coop_prepare_slot(p, &tm_q, &tm_k, &tm_v, sm, pt, flags, 1u + 2u * slot, 2u + 2u * slot);
+  const int n_prep = (int)gridDim.x - n_chain;
+  coop_prepare_slot(p, &tm_q, &tm_k, &tm_v, sm, pt, flags, 1u + 2u * slot, 2u + 2u * slot, slot,
+                    slot * n_prep + ((int)blockIdx.x - n_chain), n_prep * kCoopSlots);
 }
 
 }  // namespace

@@ -60,11 +60,12 @@ constexpr int64_t kSplitMinAvgTokens = 256;
 
 // Two kernels vs one cooperative kernel (prepare and chain overlapped in one
 // grid).  Same sweep, one sequence: the two kernels are faster at 2,048 tokens
-// (66.2 vs 80.7 us) and 4,096 (117.7 vs 123.5 us), the cooperative kernel from
-// 8,192 (213.6 vs 219.8 us; 1.42 vs 1.64 ms at 64K tokens, 2.78 vs 3.25 ms at
-// 128K).  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED use it from this average length
-// when its chains fit (coop_supported) and the workspace holds its flags.
-constexpr int64_t kCoopMinAvgTokens = 8192;
+// (63.5 vs 67.6 us), about even at 3,072 (90.1 vs 88.6 us), the cooperative
+// kernel faster from 4,096 (114.7 vs 110.6 us; 217.1 vs 197.3 us at 8K, 1.62 vs
+// 1.40 ms at 64K, 3.24 vs 2.77 ms at 128K).  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED
+// use it from this average length when its chains fit (coop_supported) and the
+// workspace holds its flags.
+constexpr int64_t kCoopMinAvgTokens = 4096;
 
 bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
   return num_seqs > 0 && total_tokens >= kSplitMinAvgTokens * num_seqs;
@@ -92,6 +93,107 @@ gdn_status attn_shape(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim
   return GDN_OK;
 }
 
+
+// Checks of a prefill call's sizes, enums and options (no pointers).  With the
+// normalisation option the chunked evaluation is the two-kernel one (the fused
+// kernel does not implement the option).
+gdn_status prefill_sizes(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
+                         int32_t d_k, int32_t d_v, gdn_dtype dtype, gdn_algo algo,
+                         uint32_t options) {
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+  if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED &&
+      algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT &&
+      algo != GDN_ALGO_CHUNKED_COOP)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  const gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  if (st != GDN_OK) return st;
+  if (total_tokens > INT32_MAX) return GDN_ERR_UNSUPPORTED_SHAPE;  // cu_seqlens is int32
+  if ((options & GDN_OPT_QK_L2NORM) && algo == GDN_ALGO_CHUNKED_FUSED) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+// The current device's SM count, or -1 if the query fails.
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return sms;
+}
+
+// Which kernels a prefill call runs, from its sizes alone (shared by
+// gdn_prefill_ex and gdn_prefill_form).  have_ws / ws_aligned: a workspace
+// pointer is given / it is 16-byte aligned; sms: the device's SM count (< 0:
+// the query failed).  Errors are those gdn_prefill returns for these sizes.
+struct Route {
+  gdn_status st = GDN_OK;
+  bool run_scan = true, run_chunk = false, split = false, coop = false;
+  int32_t min_chunk_len = INT32_MAX;
+};
+Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32_t h_k,
+                    int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype, bool qk_norm,
+                    bool have_ws, bool ws_aligned, size_t workspace_bytes, int sms) {
+  Route r;
+  auto fail = [&r](gdn_status st) {
+    r.st = st;
+    return r;
+  };
+  const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
+  const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
+                          algo == GDN_ALGO_CHUNKED_SPLIT || algo == GDN_ALGO_CHUNKED_COOP;
+  if (chunk_only && !chunk_ok)
+    return fail(dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE);
+  // Scan for sequences shorter than min_chunk_len, chunked for the rest.  With
+  // one sequence its length is total_tokens, so only the kernel with work runs.
+  if (algo == GDN_ALGO_SCAN) {
+    r.min_chunk_len = INT32_MAX;
+  } else if (chunk_only) {
+    r.min_chunk_len = 0;
+    r.run_scan = false;
+    r.run_chunk = true;
+  } else {
+    r.min_chunk_len = crossover_for(h_k, h_v, d_k, d_v, dtype);
+    r.run_chunk = chunk_ok && total_tokens >= r.min_chunk_len;
+    r.run_scan = !(num_seqs == 1 && r.run_chunk);
+  }
+  // The chunked evaluation runs as one fused kernel, as two kernels meeting in
+  // the caller's workspace (forced by GDN_ALGO_CHUNKED_SPLIT; otherwise when the
+  // sequences are long enough and the workspace is large enough), or as one
+  // cooperative kernel through the workspace.
+  if (r.run_chunk && algo == GDN_ALGO_CHUNKED_COOP) {
+    if (!have_ws) return fail(GDN_ERR_NULL_POINTER);
+    if (!ws_aligned) return fail(GDN_ERR_MISALIGNED);
+    if (workspace_bytes < gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v))
+      return fail(GDN_ERR_WORKSPACE_TOO_SMALL);
+    if (sms < 0) return fail(GDN_ERR_CUDA);
+    if (!gdn::coop_supported(num_seqs, h_v, d_v, sms)) return fail(GDN_ERR_UNSUPPORTED_SHAPE);
+    r.coop = true;
+  } else if (r.run_chunk && algo != GDN_ALGO_CHUNKED_FUSED) {
+    const size_t need = gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
+    if (algo == GDN_ALGO_CHUNKED_SPLIT) {
+      if (!have_ws) return fail(GDN_ERR_NULL_POINTER);
+      if (workspace_bytes < need) return fail(GDN_ERR_WORKSPACE_TOO_SMALL);
+    }
+    if (have_ws && !ws_aligned) return fail(GDN_ERR_MISALIGNED);
+    r.split = have_ws && workspace_bytes >= need &&
+              (algo == GDN_ALGO_CHUNKED_SPLIT || qk_norm || split_preferred(num_seqs, total_tokens));
+    if (qk_norm && !r.split) {  // no room for the two kernels: the token scan takes everything
+      if (algo == GDN_ALGO_CHUNKED) return fail(GDN_ERR_WORKSPACE_TOO_SMALL);
+      r.run_chunk = false;
+      r.run_scan = true;
+      r.min_chunk_len = INT32_MAX;
+    }
+  }
+  if (r.split && algo != GDN_ALGO_CHUNKED_SPLIT && total_tokens >= kCoopMinAvgTokens * num_seqs &&
+      workspace_bytes >= gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v) && sms > 0 &&
+      gdn::coop_supported(num_seqs, h_v, d_v, sms)) {
+    r.coop = true;
+    r.split = false;
+  }
+  return r;
+}
 }  // namespace
 
 extern "C" {
@@ -131,6 +233,22 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
   return gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v);
 }
 
+int32_t gdn_prefill_form(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
+                         int32_t d_k, int32_t d_v, gdn_dtype dtype, gdn_algo algo,
+                         size_t workspace_bytes, uint32_t options, int32_t sm_count) {
+  const gdn_status st =
+      prefill_sizes(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype, algo, options);
+  if (st != GDN_OK) return -static_cast<int32_t>(st);
+  if (num_seqs == 0) return GDN_ALGO_SCAN;  // nothing runs
+  const int sms = sm_count > 0 ? sm_count : device_sm_count();
+  const Route r = route_prefill(algo, num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype,
+                                (options & GDN_OPT_QK_L2NORM) != 0, workspace_bytes > 0, true,
+                                workspace_bytes, sms);
+  if (r.st != GDN_OK) return -static_cast<int32_t>(r.st);
+  if (!r.run_chunk) return GDN_ALGO_SCAN;
+  return r.coop ? GDN_ALGO_CHUNKED_COOP : r.split ? GDN_ALGO_CHUNKED_SPLIT : GDN_ALGO_CHUNKED_FUSED;
+}
+
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
                        const float* beta, const float* state_in, float* state_out, void* o,
                        const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
@@ -148,16 +266,8 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
                           int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, gdn_dtype dtype,
                           float scale, gdn_algo algo, void* workspace, size_t workspace_bytes,
                           uint32_t options, gdn_stream_t stream) {
-  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
-  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
-  if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_SCAN && algo != GDN_ALGO_CHUNKED &&
-      algo != GDN_ALGO_CHUNKED_FUSED && algo != GDN_ALGO_CHUNKED_SPLIT &&
-      algo != GDN_ALGO_CHUNKED_COOP)
-    return GDN_ERR_INVALID_ARG;
-  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
-  gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  gdn_status st = prefill_sizes(num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype, algo, options);
   if (st != GDN_OK) return st;
-  if (total_tokens > INT32_MAX) return GDN_ERR_UNSUPPORTED_SHAPE;  // cu_seqlens is int32
   if (num_seqs == 0) return GDN_OK;
   if (!cu_seqlens || !state_out) return GDN_ERR_NULL_POINTER;
   if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_NULL_POINTER;
@@ -172,14 +282,11 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
     if (a < b + state_bytes && b < a + state_bytes) return GDN_ERR_INVALID_ARG;
   }
   const bool qk_norm = (options & GDN_OPT_QK_L2NORM) != 0;
-  // With the normalisation option the chunked evaluation is the two-kernel one
-  // (the fused kernel does not implement the option).
-  if (qk_norm && algo == GDN_ALGO_CHUNKED_FUSED) return GDN_ERR_INVALID_ARG;
-  const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
-  const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
-                          algo == GDN_ALGO_CHUNKED_SPLIT || algo == GDN_ALGO_CHUNKED_COOP;
-  if (chunk_only && !chunk_ok)
-    return dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE;
+  const int sms = device_sm_count();
+  const Route r = route_prefill(algo, num_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype, qk_norm,
+                                workspace != nullptr, !workspace || aligned16(workspace),
+                                workspace_bytes, sms);
+  if (r.st != GDN_OK) return r.st;
 
   gdn::PrefillArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
@@ -189,63 +296,8 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
   a.dtype = dtype; a.scale = scale;
   a.qk_norm = qk_norm ? 1 : 0;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes;
-
-  // Which kernels run: scan for sequences shorter than min_chunk_len, chunked
-  // for the rest.  With one sequence its length is total_tokens, so the host
-  // can launch only the kernel that has work.
-  bool run_scan = true, run_chunk = false;
-  if (algo == GDN_ALGO_SCAN) {
-    a.min_chunk_len = INT32_MAX;
-  } else if (chunk_only) {
-    a.min_chunk_len = 0;
-    run_scan = false;
-    run_chunk = true;
-  } else {
-    a.min_chunk_len = crossover_for(h_k, h_v, d_k, d_v, dtype);
-    run_chunk = chunk_ok && total_tokens >= a.min_chunk_len;
-    run_scan = !(num_seqs == 1 && run_chunk);
-  }
-  // The chunked evaluation runs as one fused kernel, or as two kernels meeting
-  // in the caller's workspace (forced by GDN_ALGO_CHUNKED_SPLIT; otherwise when
-  // the sequences are long enough and the workspace is large enough).
-  bool split = false, coop = false;
-  if (run_chunk && algo == GDN_ALGO_CHUNKED_COOP) {
-    if (!workspace) return GDN_ERR_NULL_POINTER;
-    if (!aligned16(workspace)) return GDN_ERR_MISALIGNED;
-    if (workspace_bytes < gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v))
-      return GDN_ERR_WORKSPACE_TOO_SMALL;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    if (!gdn::coop_supported(num_seqs, h_v, d_v, sms)) return GDN_ERR_UNSUPPORTED_SHAPE;
-    coop = true;
-  } else if (run_chunk && algo != GDN_ALGO_CHUNKED_FUSED) {
-    const size_t need = gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
-    if (algo == GDN_ALGO_CHUNKED_SPLIT) {
-      if (!workspace) return GDN_ERR_NULL_POINTER;
-      if (workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
-    }
-    if (workspace && !aligned16(workspace)) return GDN_ERR_MISALIGNED;
-    split = workspace && workspace_bytes >= need &&
-            (algo == GDN_ALGO_CHUNKED_SPLIT || qk_norm || split_preferred(num_seqs, total_tokens));
-    if (qk_norm && !split) {  // no room for the two kernels: the token scan takes everything
-      if (algo == GDN_ALGO_CHUNKED) return GDN_ERR_WORKSPACE_TOO_SMALL;
-      run_chunk = false;
-      run_scan = true;
-      a.min_chunk_len = INT32_MAX;
-    }
-  }
-  if (split && algo != GDN_ALGO_CHUNKED_SPLIT && total_tokens >= kCoopMinAvgTokens * num_seqs &&
-      workspace_bytes >= gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v)) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        gdn::coop_supported(num_seqs, h_v, d_v, sms)) {
-      coop = true;
-      split = false;
-    }
-  }
+  a.min_chunk_len = r.min_chunk_len;
+  const bool run_scan = r.run_scan, run_chunk = r.run_chunk, split = r.split, coop = r.coop;
   st = error_word(&a.err);
   if (st != GDN_OK) return st;
 

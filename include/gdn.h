@@ -123,7 +123,7 @@ typedef enum {
  * GDN_ERR_WORKSPACE_TOO_SMALL without one.  The same work also runs as one
  * cooperative kernel whose prepare CTAs and state-pass CTAs overlap
  * (GDN_ALGO_CHUNKED_COOP; AUTO and CHUNKED take it when the sequences average at
- * least 8,192 tokens, its state passes fit and the workspace holds its ready
+ * least 4,096 tokens, its state passes fit and the workspace holds its ready
  * flags; its results equal the two kernels' bit for bit).  Results agree
  * within rounding; the
  * workspace is not used after the launches complete.
@@ -382,6 +382,23 @@ gdn_status gdn_stream_status(gdn_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* gdn_status_string(gdn_status status);
+
+/*
+ * gdn_prefill_form — which evaluation gdn_prefill / gdn_prefill_ex would run
+ * for these sizes, algorithm, workspace size (0: no workspace) and options,
+ * without launching anything: GDN_ALGO_SCAN when only the token scan runs, else
+ * the form of the chunked evaluation of the sequences at or above the
+ * crossover (GDN_ALGO_CHUNKED_FUSED, GDN_ALGO_CHUNKED_SPLIT or
+ * GDN_ALGO_CHUNKED_COOP; with more than one sequence the shorter ones still
+ * take the scan).  sm_count is the device's SM count (0: query the current
+ * device).  On arguments the call would refuse it returns the negated status
+ * (-GDN_ERR_...).  The cooperative form is reported when the call would try
+ * it; if the device then refuses the cooperative launch (other work holds
+ * SMs), AUTO and CHUNKED run the two kernels instead.
+ */
+int32_t gdn_prefill_form(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
+                         int32_t d_k, int32_t d_v, gdn_dtype dtype, gdn_algo algo,
+                         size_t workspace_bytes, uint32_t options, int32_t sm_count);
 
 /*
  * gdn_prefill_crossover_tokens — the sequence length at and above which

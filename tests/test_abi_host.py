@@ -258,3 +258,46 @@ def test_prefill_from_host_memory_errors(lib):
     assert lib.gdn_prefill_host_workspace_size(100, 16, 32, 128, 128, 1) == 0
     # grows with the piece, not with the prompt
     assert lib.gdn_prefill_host_workspace_size(2048, 16, 32, 128, 128, 1) > need
+
+
+def test_prefill_form_query(lib):
+    """gdn_prefill_form reports the evaluation a call would run, from sizes alone
+    (the SM count given, so no device is needed)."""
+    S = 152  # SMs of a GB300
+
+    def form(n, t, algo=0, ws=None, opt=0, sms=S, d_v=128, dtype=1):
+        if ws is None:
+            ws = lib.gdn_prefill_workspace_size(n, t, 16, 32, 128, d_v, dtype, algo)
+        return lib.gdn_prefill_form(n, t, 16, 32, 128, d_v, dtype, algo, ws, opt, sms)
+
+    SCAN, FUSED, SPLIT, COOP = 1, 3, 4, 5
+    x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
+    assert form(1, x - 1) == SCAN                       # below the crossover: token scan
+    assert form(1, 200) == FUSED                        # short: the fused kernel, no workspace
+    assert form(1, 2048) == SPLIT                       # two kernels
+    assert form(1, 4096) == COOP                        # from 4,096 tokens: cooperative
+    assert form(1, 4096, ws=0) == FUSED                 # no workspace: the fused kernel
+    split_ws = lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4)
+    assert form(1, 4096, ws=split_ws) == SPLIT          # no room for the ready flags
+    assert form(1, 4096, sms=64) == SPLIT               # 64 state passes need > 96 SMs
+    # state passes of 64 rows: 2 x 32 x 2 = 128 are more than two thirds of the SMs
+    assert form(2, 2 * 4096) == SPLIT
+    ws8 = lib.gdn_prefill_workspace_size(4, 4 * 4096, 4, 8, 128, 128, 1, 0)
+    assert lib.gdn_prefill_form(4, 4 * 4096, 4, 8, 128, 128, 1, 0, ws8, 0, S) == COOP  # 64 passes
+    assert lib.gdn_prefill_form(4, 4 * 3000, 4, 8, 128, 128, 1, 0, ws8, 0, S) == SPLIT  # shorter
+    assert form(1, 4096, algo=4) == SPLIT               # forced forms
+    assert form(1, 2048, algo=5) == COOP
+    assert form(1, 4096, algo=3) == FUSED
+    assert form(1, 4096, algo=1) == SCAN
+    assert form(1, 4096, opt=1, ws=0) == SCAN           # normalisation without room: scan
+    assert form(1, 4096, d_v=16, ws=1 << 30) == SCAN    # d_v below the chunked kernels' 32
+    assert form(0, 0) == SCAN                           # nothing runs
+    # refusals come back negated
+    assert form(1, 4096, algo=5, ws=0) == -1            # the cooperative form needs a workspace
+    assert form(1, 4096, algo=5, ws=1024) == -7
+    assert form(1, 4096, algo=4, ws=0) == -1
+    assert form(1, 4096, algo=3, opt=1) == -2           # fused kernel has no normalisation
+    assert form(1, 4096, algo=2, dtype=0) == -4         # fp32 has no chunked evaluation
+    assert form(1, 4096, algo=9) == -2
+    assert form(-1, 4096) == -2
+    assert lib.gdn_prefill_form(1, 4096, 16, 30, 128, 128, 1, 0, 0, 0, S) == -3
