@@ -403,7 +403,8 @@ def main():
     dq = inputs.make_prefill(lengths, h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"] + n0 + 1,
                              unit_qk=False)
     xq = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dq.items()}
-    ws_q_algo = args.algo if args.algo in ("chunked_split", "chunked_coop") else "chunked_split"
+    # the same evaluation as the step above (AUTO's workspace holds the cooperative form)
+    ws_q_algo = args.algo if args.algo != "scan" else "chunked_split"
     ws_q = torch.empty(max(gdn_prefill_workspace_size(1, T, h_k, h_v, d_k, d_v, torch.bfloat16,
                                                       ws_q_algo), 16),
                        dtype=torch.uint8, device=dev)
