@@ -20,7 +20,8 @@
 // chunk_chain_kernel walks each (sequence, value head, 32-row slice of d_v) in
 // chunk order with the fp32 state in TMEM, bulk-copying the packages into a
 // 3-stage ring next to the TMA'd Q and K:
-//   D = [-W; Q] S^T,  U = U~ + D_top,
+//   D = [U~; 0] + [-W; Q] S^T  (the product accumulates onto a buffer preloaded
+//                               with U~, so D_top is U itself),
 //   S^T <- Gamma_n S^T + K^T (decay U),  O = Gamma D_bottom + P U.
 // Warp roles: a producer warp (copies), an MMA warp (one thread issues every
 // product; an issue blocks while the tensor pipe is busy, so it gets a warp of
@@ -725,9 +726,9 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
       if (tc::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // D = [-W; Q] S_s^T
+        for (int kk = 0; kk < 8; ++kk)  // D = [U~; 0] + [-W; Q] S_s^T (preloaded buffer)
           tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
-                       dSS + ((kk * 1024) >> 4), CF::IDC_WQ, kk > 0);
+                       dSS + ((kk * 1024) >> 4), CF::IDC_WQ, 1);
         tc::mma_commit(bar_d);
       }
       __syncwarp();
@@ -814,32 +815,19 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       tc::fence_before_sync();
       tc::mbar_arrive(bar_ss);
     };
-    {  // initial state: rows 32 b0 .. of the slice, column jrow
-      float sc[32 * BPW];
-#pragma unroll
-      for (int i = 0; i < 32 * BPW; ++i)
-        sc[i] = p.state_in ? p.state_in[(srow0 + 32 * b0 + i) * kDK + jrow] : 0.f;
-      if (nchunks == 0) {
-#pragma unroll
-        for (int i = 0; i < 32 * BPW; ++i) p.state_out[(srow0 + 32 * b0 + i) * kDK + jrow] = sc[i];
-      } else {
-        stage_state(sc, 0);
-      }
-    }
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % NSTG;
-      const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
-      if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
-        ok = tc::mbar_wait(bar_d, c & 1) && ok;
-        // U~ arrived by bulk copy: observe the stage's own barrier before reading it
-        ok = tc::mbar_wait(&full[st], (c / NSTG) & 1) && ok;
-        tc::fence_after_sync();
-        const float dec_r = gates[64 + rl];
+    // D of chunk cn accumulates onto its TMEM buffer, preloaded with U~ in rows
+    // 0-63 (by the warps on those lanes) and zeros in rows 64-127 (the output
+    // warps), so that U = U~ - W S^T comes out of the product itself.  Written
+    // before the warps stage the state that D waits for; off the critical path.
+    auto preload = [&](int cn) {
+      const int stn = cn % NSTG;
+      const uint32_t td = tmem + lane_base + CF::TC_D0 + DVS * (cn & 1);
+      float u[32];
+      if ((warp & 3) < 2) {
+        ok = tc::mbar_wait(&full[stn], (cn / NSTG) & 1) && ok;  // U~ arrived by bulk copy
 #pragma unroll
         for (int b = b0; b < b0 + BPW; ++b) {
-          float u[32], d[32];
-          tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c & 1) + 32 * b, d);
-          const uint8_t* ut = smem + st * CF::kMain + SC_U + b * kPkgUSlice;  // row of U~, bf16
+          const uint8_t* ut = smem + stn * CF::kMain + SC_U + b * kPkgUSlice;  // row of U~, bf16
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint4 q4 =
@@ -851,8 +839,39 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
               u[8 * j + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
             }
           }
+          tc::tmem_st32(td + 32 * b, u);
+        }
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] += d[i];
+        for (int i = 0; i < 32; ++i) u[i] = 0.f;
+#pragma unroll
+        for (int b = b0; b < b0 + BPW; ++b) tc::tmem_st32(td + 32 * b, u);
+      }
+    };
+    {  // initial state: rows 32 b0 .. of the slice, column jrow
+      float sc[32 * BPW];
+#pragma unroll
+      for (int i = 0; i < 32 * BPW; ++i)
+        sc[i] = p.state_in ? p.state_in[(srow0 + 32 * b0 + i) * kDK + jrow] : 0.f;
+      if (nchunks == 0) {
+#pragma unroll
+        for (int i = 0; i < 32 * BPW; ++i) p.state_out[(srow0 + 32 * b0 + i) * kDK + jrow] = sc[i];
+      } else {
+        preload(0);
+        stage_state(sc, 0);
+      }
+    }
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c % NSTG;
+      const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
+      if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
+        ok = tc::mbar_wait(bar_d, c & 1) && ok;
+        tc::fence_after_sync();
+        const float dec_r = gates[64 + rl];
+#pragma unroll
+        for (int b = b0; b < b0 + BPW; ++b) {
+          float u[32];
+          tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c & 1) + 32 * b, u);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
             st_chunk<2>(smem + CF::CC_UB + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
@@ -865,8 +884,10 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         tc::fence_proxy_async();
         tc::fence_before_sync();
         tc::mbar_arrive(bar_u);
-      } else if (c > 0) {
-        finish_output(c - 1);  // warps 2-3, while U is formed
+        if (c + 1 < nchunks) preload(c + 1);  // while the state update runs
+      } else {
+        if (c > 0) finish_output(c - 1);  // warps 2-3, while U is formed
+        if (c + 1 < nchunks) preload(c + 1);  // after that output read the buffer's rows
       }
       ok = tc::mbar_wait(bar_s, c & 1) && ok;
       tc::fence_after_sync();
