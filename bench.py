@@ -40,11 +40,11 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "2d02727ca58fd2d4",
-                    "bytes": (68_260_608 + 31_671_808) + (118_790_400 + 12_266_240),
+                    "sha256_16": "7ef0d90f11b2e111",
+                    "bytes": (68_253_696 + 31_597_824) + (118_793_216 + 12_335_616),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                   "sha256_16": "2d02727ca58fd2d4", "bytes": 68_684_288 + 67_595_264,
+                   "sha256_16": "7ef0d90f11b2e111", "bytes": 68_625_920 + 66_269_440,
                    "profile": "profiles/chunk_coop_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
