@@ -28,7 +28,8 @@
 // its own) and four epilogue warps, handing over through mbarriers.  Only D,
 // U, the state update and the state's staging are on the chunk-to-chunk
 // critical path: P U of chunk c runs while chunk c's state is staged, and
-// chunk c's output is written while chunk c+1's U is formed.
+// chunk c's output is written once chunk c+2's state is staged (D and P U are
+// triple-buffered in TMEM), away from the U epilogue and the state staging.
 // chunk_plan_kernel computes each sequence's first package index (an exclusive
 // prefix sum of its chunk count) into the workspace header and records an
 // inconsistent cu_seqlens in the error word.
@@ -566,7 +567,7 @@ struct ChainCfg {
   static constexpr uint32_t CC_MISC = CC_GATE + NSTG * kGateBytes;
   static constexpr uint32_t kSmem = CC_MISC + 256 + 1024;
   static constexpr uint32_t kTmemCols = DVS == 32 ? 256 : 512;
-  static constexpr uint32_t TC_D0 = 0, TC_O0 = 2 * DVS, TC_S = 4 * DVS;  // D, P U double-buffered
+  static constexpr uint32_t TC_D0 = 0, TC_O0 = 3 * DVS, TC_S = 6 * DVS;  // D, P U triple-buffered
   static constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, DVS, false, true);  // [-W; Q] S^T
   static constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, DVS, true, true);   // K^T (decay U)
   static constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, DVS, false, true);  // [.; P] U
@@ -577,7 +578,7 @@ struct ChainCfg {
   static_assert(kMain % 1024 == 0 && kTail % 1024 == 0 && CC_TAIL % 1024 == 0 &&
                     CC_SS % 1024 == 0 && SC_U % 512 == 0,
                 "swizzled operands need 1024 / 512 byte alignment");
-  static_assert(5 * DVS <= (int)kTmemCols, "TMEM columns");
+  static_assert(7 * DVS <= (int)kTmemCols, "TMEM columns");
 };
 
 // Bounded wait for a prepare item's ready flag (stored with release semantics
@@ -636,8 +637,8 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   uint64_t* bar_s = bar_d + 1;
   uint64_t* bar_u = bar_s + 1;
   uint64_t* bar_ss = bar_u + 1;
-  uint64_t* bar_o = bar_ss + 1;  // one per chunk parity
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
+  uint64_t* bar_o = bar_ss + 1;  // one per chunk modulo 3
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 3);
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, CF::kTmemCols);
     tc::tmem_relinquish();
@@ -653,8 +654,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_u, 2 * kEpiThreads / 4);
     tc::mbar_init(bar_ss, kEpiThreads);
-    tc::mbar_init(&bar_o[0], 1);
-    tc::mbar_init(&bar_o[1], 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&bar_o[i], 1);
     tc::fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -722,7 +722,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       const int st = c % NSTG;
       const uint64_t so = (uint64_t)((st * CF::kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
       const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
-      const uint32_t td = tmem + CF::TC_D0 + DVS * (c & 1), to2 = tmem + CF::TC_O0 + DVS * (c & 1);
+      const uint32_t td = tmem + CF::TC_D0 + DVS * (c % 3), to2 = tmem + CF::TC_O0 + DVS * (c % 3);
       if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
       if (tc::elect_one()) {
 #pragma unroll
@@ -747,7 +747,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
           tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), CF::IDC_PU, kk > 0);
-        tc::mma_commit(&bar_o[c & 1]);
+        tc::mma_commit(&bar_o[c % 3]);
       }
       __syncwarp();
     }
@@ -756,24 +756,34 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     // write the previous chunk's output meanwhile; all stage the state.  Every
     // hand-off is an mbarrier with a bounded wait.
     const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
-    // Output of chunk cp (warps 2-3): O = Gamma Q S^T + P U for rows r = lanes
-    // 64-127, then release its tail stage.
-    auto finish_output = [&](int cp) {
+    // Output of chunk cp (the warps on lanes 64-127): O = Gamma Q S^T + P U, in
+    // two parts.  take_gates(cp) waits for P U, reads the rows' output factors
+    // and releases the chunk's tail stage early, so that the next tail copy has
+    // time to land; write_output(cp) forms and stores the rows after the next
+    // state has been staged, so that its global stores neither compete with the
+    // U warps' shared-memory stores nor delay the state (D and P U are
+    // triple-buffered in TMEM for that).
+    auto take_gates = [&](int cp) {
       const int stp = cp % NSTG;
-      const float* gp = reinterpret_cast<const float*>(smem + CF::CC_GATE + stp * kGateBytes);
-      // P U of chunk cp + 2 is issued only after this chunk's output is done
-      // (warps 2-3 then stage chunk cp + 1's state), so the parity is unambiguous
-      ok = tc::mbar_wait(&bar_o[cp & 1], (cp >> 1) & 1) && ok;
+      // P U of chunk cp + 3 is issued only after these warps stage chunk cp + 3's
+      // state, later than this wait, so the phase parity is unambiguous
+      ok = tc::mbar_wait(&bar_o[cp % 3], (cp / 3) & 1) && ok;
       tc::fence_after_sync();
+      const float gr =
+          reinterpret_cast<const float*>(smem + CF::CC_GATE + stp * kGateBytes)[rl];
+      tc::fence_before_sync();
+      tc::mbar_arrive(&tempty[stp]);
+      return gr;
+    };
+    auto write_output = [&](int cp, float Gam_r) {
       const int64_t t0p = t_beg + (int64_t)cp * kC;
       const int nvp = (int)((L - (int64_t)cp * kC) < kC ? (L - (int64_t)cp * kC) : kC);
 #pragma unroll
       for (int b = b0; b < b0 + BPW; ++b) {
         float o1[32], o2[32];
-        tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (cp & 1) + 32 * b, o1);
-        tc::tmem_ld32(tmem + lane_base + CF::TC_O0 + DVS * (cp & 1) + 32 * b, o2);
+        tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (cp % 3) + 32 * b, o1);
+        tc::tmem_ld32(tmem + lane_base + CF::TC_O0 + DVS * (cp % 3) + 32 * b, o2);
         if (rl < nvp) {
-          const float Gam_r = gp[rl];
 #pragma unroll
           for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
           uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0p + rl) * p.h_v + h) * (int64_t)p.d_v +
@@ -789,8 +799,6 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
           }
         }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(&tempty[stp]);
     };
     // S (fp32, thread j holds column j of the slice) -> bf16 operand copy for
     // chunk cn's D, then Gamma_n of chunk cn applied in TMEM (the update MMA
@@ -821,7 +829,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     // before the warps stage the state that D waits for; off the critical path.
     auto preload = [&](int cn) {
       const int stn = cn % NSTG;
-      const uint32_t td = tmem + lane_base + CF::TC_D0 + DVS * (cn & 1);
+      const uint32_t td = tmem + lane_base + CF::TC_D0 + DVS * (cn % 3);
       float u[32];
       if ((warp & 3) < 2) {
         ok = tc::mbar_wait(&full[stn], (cn / NSTG) & 1) && ok;  // U~ arrived by bulk copy
@@ -861,6 +869,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         stage_state(sc, 0);
       }
     }
+    float gam_prev = 0.f;  // output factor of the previous chunk's rows (output warps)
     for (int c = 0; c < nchunks && ok; ++c) {
       const int st = c % NSTG;
       const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
@@ -871,7 +880,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
 #pragma unroll
         for (int b = b0; b < b0 + BPW; ++b) {
           float u[32];
-          tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c & 1) + 32 * b, u);
+          tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c % 3) + 32 * b, u);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
             st_chunk<2>(smem + CF::CC_UB + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
@@ -886,8 +895,8 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         tc::mbar_arrive(bar_u);
         if (c + 1 < nchunks) preload(c + 1);  // while the state update runs
       } else {
-        if (c > 0) finish_output(c - 1);  // warps 2-3, while U is formed
-        if (c + 1 < nchunks) preload(c + 1);  // after that output read the buffer's rows
+        if (c > 0) gam_prev = take_gates(c - 1);
+        if (c + 1 < nchunks) preload(c + 1);  // the buffer's rows were read by output c - 2
       }
       ok = tc::mbar_wait(bar_s, c & 1) && ok;
       tc::fence_after_sync();
@@ -902,8 +911,10 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       } else {
         stage_state(sc, c + 1);
       }
+      if ((warp & 3) >= 2 && c > 0) write_output(c - 1, gam_prev);  // after the staging
     }
-    if (ok && nchunks > 0 && (warp & 3) >= 2) finish_output(nchunks - 1);  // the last output
+    if (ok && nchunks > 0 && (warp & 3) >= 2)  // the last output
+      write_output(nchunks - 1, take_gates(nchunks - 1));
   }
   if (!ok) raise_error(p.err, kErrDeviceTimeout);
   tc::fence_before_sync();
