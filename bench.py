@@ -40,11 +40,11 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "7ef0d90f11b2e111",
-                    "bytes": (68_253_696 + 31_597_824) + (118_793_216 + 12_335_616),
+                    "sha256_16": "66ba0d5189080d55",
+                    "bytes": (68_254_720 + 31_455_488) + (118_787_840 + 11_955_968),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                   "sha256_16": "7ef0d90f11b2e111", "bytes": 68_625_920 + 66_269_440,
+                   "sha256_16": "66ba0d5189080d55", "bytes": 68_641_792 + 67_524_352,
                    "profile": "profiles/chunk_coop_t4096.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
