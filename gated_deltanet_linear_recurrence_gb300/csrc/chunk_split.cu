@@ -626,9 +626,10 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * DVS;
 
   // mbarriers.  full/tfull: TMA and bulk copies landed; empty: the stage's MMAs
-  // are done (tcgen05.commit); tempty: warps 2-3 wrote the chunk's output.
-  // bar_d, bar_s, bar_o: D, the state update, P U complete (tcgen05.commit);
-  // bar_u: warps 0-1 staged U; bar_ss: warps 0-3 staged the state.
+  // are done (tcgen05.commit); tempty: the output warps took the chunk's gates.
+  // bar_d, bar_s, bar_o: D, the state update, P U complete (tcgen05.commit;
+  // bar_o one per chunk modulo 3); bar_u: the U warps staged U; bar_ss: every
+  // epilogue warp staged the state.
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + CF::CC_MISC);
   uint64_t* empty = full + NSTG;
   uint64_t* tfull = empty + NSTG;
@@ -752,9 +753,11 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       __syncwarp();
     }
   } else if (warp < EW) {
-    // Epilogue warps.  Those on TMEM lanes 0-63 form U; those on lanes 64-127
-    // write the previous chunk's output meanwhile; all stage the state.  Every
-    // hand-off is an mbarrier with a bounded wait.
+    // Epilogue warps.  Those on TMEM lanes 0-63 form U and preload the next
+    // chunk's U~; those on lanes 64-127 take the previous chunk's gates, clear
+    // rows 64-127 of the next D buffer and, once the state is staged, store the
+    // previous chunk's output; all stage the state.  Every hand-off is an
+    // mbarrier with a bounded wait.
     const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
     // Output of chunk cp (the warps on lanes 64-127): O = Gamma Q S^T + P U, in
     // two parts.  take_gates(cp) waits for P U, reads the rows' output factors
