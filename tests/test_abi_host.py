@@ -301,3 +301,23 @@ def test_prefill_form_query(lib):
     assert form(1, 4096, algo=9) == -2
     assert form(-1, 4096) == -2
     assert lib.gdn_prefill_form(1, 4096, 16, 30, 128, 128, 1, 0, 0, 0, S) == -3
+
+
+def test_prefill_form_python_names():
+    """The Python wrapper maps the query's answer to the algorithm names that
+    gdn_prefill takes, and raises GdnError for refused arguments."""
+    import torch
+    from gated_deltanet_linear_recurrence_gb300 import (GdnError, gdn_prefill_form,
+                                                        gdn_prefill_workspace_size)
+
+    ws = gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, torch.bfloat16)
+    f = lambda t, **kw: gdn_prefill_form(1, t, 16, 32, 128, 128, torch.bfloat16, sm_count=152, **kw)
+    assert f(4096, workspace_bytes=ws) == "chunked_coop"
+    assert f(2048, workspace_bytes=ws) == "chunked_split"
+    assert f(4096) == "chunked_fused"
+    assert f(4, workspace_bytes=ws) == "scan"
+    assert f(4096, algo="chunked_split", workspace_bytes=ws) == "chunked_split"
+    with pytest.raises(GdnError):
+        f(4096, algo="chunked_coop")          # no workspace
+    with pytest.raises(GdnError):
+        f(4096, algo="chunked_fused", qk_l2norm=True)
