@@ -61,10 +61,10 @@ constexpr int64_t kSplitMinAvgTokens = 256;
 // Two kernels vs one cooperative kernel (prepare and chain overlapped in one
 // grid).  Same sweep, one sequence: the two kernels are faster at 2,048 tokens
 // (63.5 vs 67.6 us), about even at 3,072 (90.1 vs 88.6 us), the cooperative
-// kernel faster from 4,096 (114.7 vs 110.6 us; 217.1 vs 197.3 us at 8K, 1.62 vs
-// 1.40 ms at 64K, 3.24 vs 2.77 ms at 128K).  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED
-// use it from this average length when its chains fit (coop_supported) and the
-// workspace holds its flags.
+// kernel faster from 4,096 (110.5 vs 104.4 us with the current state pass;
+// 395.6 vs 344.9 us at 16K, 3.08 vs 2.58 ms at 128K).  GDN_ALGO_AUTO and
+// GDN_ALGO_CHUNKED use it from this average length when its chains fit
+// (coop_supported) and the workspace holds its flags.
 constexpr int64_t kCoopMinAvgTokens = 4096;
 
 bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
@@ -92,7 +92,6 @@ gdn_status attn_shape(int32_t batch, int32_t h_q, int32_t h_kv, int32_t head_dim
     return GDN_ERR_UNSUPPORTED_SHAPE;
   return GDN_OK;
 }
-
 
 // Checks of a prefill call's sizes, enums and options (no pointers).  With the
 // normalisation option the chunked evaluation is the two-kernel one (the fused
@@ -194,6 +193,7 @@ Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32
   }
   return r;
 }
+
 }  // namespace
 
 extern "C" {
