@@ -18,7 +18,7 @@ __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspac
            "gdn_attn_decode_workspace_size", "gdn_attn_decode_block_keys",
            "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens",
-           "gdn_prefill_form", "GdnError",
+           "gdn_prefill_form", "gdn_selftest_wait_timeout", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
 NOALLOC_SCRATCH_BYTES = 96 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
@@ -339,3 +339,11 @@ def gdn_attn_decode(q, k_cache, v_cache, cache_len, scale=None, o=None, layout="
 def gdn_stream_status(stream=None):
     """Synchronise the stream; return (and clear) the device error word as a status name."""
     return STATUS_NAMES.get(int(_lib.load().gdn_stream_status(_stream(stream))), "unknown")
+
+
+def gdn_selftest_wait_timeout(timeout_us=1000, stream=None):
+    """Enqueue the bounded-wait self-test (see gdn_selftest_wait_timeout in
+    include/gdn.h): a device wait that expires and records GDN_ERR_DEVICE_TIMEOUT,
+    which the next gdn_stream_status reports."""
+    _lib.check(_lib.load().gdn_selftest_wait_timeout(int(timeout_us), _stream(stream)),
+               "gdn_selftest_wait_timeout")

@@ -57,6 +57,7 @@ SIGNATURES = {
     "gdn_attn_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, ctypes.c_int, _i32]),
     "gdn_attn_decode_block_keys": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.c_int, _i32]),
     "gdn_stream_status": (ctypes.c_int, [_vp]),
+    "gdn_selftest_wait_timeout": (ctypes.c_int, [_i32, _vp]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_prefill_crossover_tokens": (_i32, [_i32, _i32, _i32, _i32, ctypes.c_int]),
     "gdn_prefill_form": (_i32, [_i32, _i64, _i32, _i32, _i32, _i32, ctypes.c_int, ctypes.c_int,

@@ -446,6 +446,17 @@ gdn_status gdn_attn_decode(const void* q, const void* k_cache, const void* v_cac
   return GDN_OK;
 }
 
+gdn_status gdn_selftest_wait_timeout(int32_t timeout_us, gdn_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return GDN_ERR_INVALID_ARG;
+  int* err = nullptr;
+  const gdn_status st = error_word(&err);
+  if (st != GDN_OK) return st;
+  if (gdn::launch_selftest_wait((uint64_t)timeout_us * 1000u, err,
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
 gdn_status gdn_stream_status(gdn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GDN_ERR_CUDA;

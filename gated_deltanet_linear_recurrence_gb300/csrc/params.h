@@ -117,5 +117,7 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
 size_t coop_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v);
 bool coop_supported(int32_t num_seqs, int32_t h_v, int32_t d_v, int sm_count);
 cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStream_t stream);
+// One CTA whose bounded mbarrier wait expires (selftest.cu).
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* err, cudaStream_t stream);
 
 }  // namespace gdn

@@ -380,6 +380,18 @@ int32_t gdn_attn_decode_block_keys(int32_t batch, int32_t h_q, int32_t h_kv, int
  */
 gdn_status gdn_stream_status(gdn_stream_t stream);
 
+/*
+ * gdn_selftest_wait_timeout — a check of the library's failure path that
+ * needs no fault: one CTA on `stream` waits, with the bounded mbarrier wait
+ * every tensor-core kernel here uses for its hand-offs, on a barrier that
+ * nothing completes.  The wait gives up after timeout_us microseconds
+ * (1 .. 1,000,000), the kernel records GDN_ERR_DEVICE_TIMEOUT in the device
+ * error word and returns; the next gdn_stream_status on the stream reports
+ * and clears it, and the context stays usable.  Returns GDN_ERR_INVALID_ARG
+ * for a timeout outside the range, GDN_ERR_CUDA if the launch fails.
+ */
+gdn_status gdn_selftest_wait_timeout(int32_t timeout_us, gdn_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* gdn_status_string(gdn_status status);
 
