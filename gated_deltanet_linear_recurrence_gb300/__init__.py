@@ -108,9 +108,12 @@ def gdn_prefill(q, k, v, g, beta, cu_seqlens, state_in=None, state_out=None, o=N
         state_out = torch.empty((N, h_v, d_v, d_k), dtype=torch.float32, device=q.device)
     if state_in is not None:
         _require(state_in.dtype == torch.float32 and state_in.is_contiguous(), "state_in fp32")
-    # with the normalisation option the chunked form is the two-kernel one
-    ws_algo = "chunked_split" if (qk_l2norm and algo in ("auto", "chunked")) else algo
-    need = lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt, _lib.ALGOS[ws_algo])
+    need = lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt, _lib.ALGOS[algo])
+    if qk_l2norm and algo in ("auto", "chunked"):
+        # the normalisation option needs a workspace form (two kernels, or the
+        # cooperative one when AUTO's size query already leaves room for it)
+        need = max(need, lib.gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, dt,
+                                                        _lib.ALGOS["chunked_split"]))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
