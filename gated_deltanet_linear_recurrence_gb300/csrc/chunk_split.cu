@@ -15,7 +15,9 @@
 //   [ P ]                      bf16 [r][i], 8 KB   (e^{gamma_r - gamma_i} q_r.k_i, i <= r)
 //   [ U~ slices 0..3 ]         bf16 [r][32 values of d_v], 64-byte rows with the
 //                              SW64 XOR pattern, 4 x 4 KB  (U~ = T diag(beta) V)
-//   [ gates ]                  fp32 Gamma[64], decay[64] (e^{gamma_n - gamma_r}), Gamma_n
+//   [ gates ]                  fp32 Gamma_r / |q_r| [64], decay_r / |k_r| [64]
+//                              (decay_r = e^{gamma_n - gamma_r}; |.| = 1 without the
+//                              normalisation option), Gamma_n
 //
 // chunk_chain_kernel walks each (sequence, value head, 32-row slice of d_v) in
 // chunk order with the fp32 state in TMEM, bulk-copying the packages into a
@@ -41,7 +43,7 @@
 // chunk_coop_kernel runs the same two parts in one cooperative grid, every CTA
 // resident: prepare slots publish a ready flag per package and the state passes
 // (64 rows of a head per CTA) follow them chunk by chunk, so the two overlap
-// instead of running one after the other; it pays off on long prompts.
+// instead of running one after the other (the faster form from 4,096 tokens).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
