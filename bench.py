@@ -118,13 +118,20 @@ def prefill_bytes(T, N, h_k, h_v, d_k, d_v, esize, state_in):
 
 
 def chunked_flops_per_token(h_k, h_v, d_k, d_v, C=64):
-    """Dense MMA work the chunked form issues (2 flop per multiply-add):
-    per (chunk, key head) K K^T and Q K^T; per (chunk, value head) W, U~ and
-    P U (C x C x d products), W S^T, Q S^T and the state update (C x d_k x d_v),
-    and the triangular solve (C^3/3 multiply-adds)."""
+    """Dense tensor-core work of the chunked form per token (2 flop per
+    multiply-add): per (chunk, key head) K K^T and Q K^T; per (chunk, value
+    head) W, U~ and P U (C x C x d products), W S^T, Q S^T and the state update
+    (C x d_k x d_v).  This is the GEMM portion the roofline is stated on; the
+    triangular solve is counted apart (solve_flops_per_token)."""
     per_key = 2 * (2 * C * C * d_k)
-    per_val = 2 * C * C * d_k + 2 * 2 * C * C * d_v + 3 * (2 * C * d_k * d_v) + 2 * C ** 3 // 3
+    per_val = 2 * C * C * d_k + 2 * 2 * C * C * d_v + 3 * (2 * C * d_k * d_v)
     return (h_k * per_key + h_v * per_val) / C
+
+
+def solve_flops_per_token(h_v, C=64):
+    """The 64 x 64 unit-lower-triangular inverse per (chunk, value head):
+    C^3 / 3 multiply-adds, mostly on CUDA cores."""
+    return h_v * (2 * C ** 3 // 3) / C
 
 
 def scan_flops_per_token(h_v, d_k, d_v):
@@ -273,6 +280,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--no-long-prefill", action="store_true",
+                    help="skip the 128K-token and ten-prompt varlen prefill timings")
     ap.add_argument("--sweep", action="store_true",
                     help="time the token scan and the chunked prefill over sequence lengths "
                          "(one sequence, 16 key / 32 value heads of 128, bf16) and print the "
@@ -280,7 +289,8 @@ def main():
     ap.add_argument("--stream", action="store_true",
                     help="time the 128K-token prompt as one call and as streamed pieces "
                          "(gdn_prefill_streamed), with the workspace each needs, as JSON lines")
-    ap.add_argument("--kernel-only", choices=["prefill", "decode_b256", "attn_b1_l131072",
+    ap.add_argument("--kernel-only", choices=["prefill", "prefill_t131072", "prefill_varlen10",
+                                              "decode_b256", "attn_b1_l131072",
                                               "attn_b64_l8192"], default=None,
                     help="run only this kernel's workload (warmup + steps launches, no JSON); "
                          "for profiler captures")
@@ -377,6 +387,7 @@ def main():
     if algo_used.startswith("chunked"):
         flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
+        flop_solve = solve_flops_per_token(h_v) * T
         scope, traffic_key = {
             "chunked_coop": ("the whole gdn_prefill call: one cooperative kernel, prepare slots "
                              "and state passes overlapped (profiles/)", "chunk_coop"),
@@ -387,7 +398,10 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                 "traffic": ncu_traffic(traffic_key), "scope": scope,
                 "peak_source": f"{peaks['source']} bf16 dense (burst)",
-                "algorithmic_flop_per_launch": flop}
+                "algorithmic_flop_per_launch": flop,
+                "flop_count": "GEMM products only, 5,242,880 flop/token at 16/32 heads of 128",
+                "frac_with_solve": (flop + flop_solve) / (ms_per_step / 1e3) / 1e12
+                / peaks["bf16_tflops"]}
     else:
         flop = scan_flops_per_token(h_v, d_k, d_v) * T
         achieved = flop / (ms_per_step / 1e3) / 1e12
@@ -480,6 +494,12 @@ def main():
     if not args.no_attention:
         attention = bench_attention(torch, inputs, dev, stream, peaks, args, flush)
 
+    long_prefill = {}
+    if not args.no_long_prefill:
+        for name in ("prefill_t131072", "prefill_varlen10"):
+            long_prefill[name] = bench_prefill_workload(torch, inputs, name, dev, stream, peaks,
+                                                        args, flush)
+
     clk = clocks.stop()
     assert gdn_stream_status(stream) == "GDN_OK"
 
@@ -502,6 +522,8 @@ def main():
         "clocks": clk,
         "decode": decode,
         "attn_decode": attention,
+        "prefill_t131072": long_prefill.get("prefill_t131072"),
+        "prefill_varlen10": long_prefill.get("prefill_varlen10"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, w)
@@ -509,6 +531,69 @@ def main():
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def bench_prefill_workload(torch, inputs, name, dev, stream, peaks, args, flush):
+    """AUTO on one of the long prefill workloads (the 128K-token prompt with a
+    drawn initial state; the ten packed prompts of 256 ... 128K tokens): ms per
+    call and tok/s with inputs resident and L2 flushed before each call, the
+    form the library ran, and the roofline of that call (survey flop count,
+    measured bf16 peak; DRAM traffic from the matching ncu capture while the
+    kernels' sources are unchanged, else null)."""
+    from gated_deltanet_linear_recurrence_gb300 import (gdn_prefill, gdn_prefill_form,
+                                                        gdn_prefill_workspace_size)
+    w = inputs.WORKLOADS[name]
+    h_k, h_v, d_k, d_v = w["h_k"], w["h_v"], w["d_k"], w["d_v"]
+    d = inputs.make_prefill(w["lengths"], h_k, h_v, d_k, d_v, w["dtype"], seed=w["seed"],
+                            state_std=w["state_std"])
+    x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    del d
+    T, N = sum(w["lengths"]), len(w["lengths"])
+    o = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((N, h_v, d_v, d_k), dtype=torch.float32, device=dev)
+    ws_n = gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v, torch.bfloat16, "auto")
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    form = gdn_prefill_form(N, T, h_k, h_v, d_k, d_v, torch.bfloat16, "auto", ws_n)
+
+    def once():
+        gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
+                    state_in=x["state_in"], state_out=st, o=o, algo="auto", workspace=ws,
+                    stream=stream)
+
+    for _ in range(args.warmup):
+        flush()
+        once()
+    ts = []
+    for _ in range(max(args.steps // 2, 5)):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        once()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    flop = chunked_flops_per_token(h_k, h_v, d_k, d_v) * T
+    tflops = flop / (ms / 1e3) / 1e12
+    nbytes = prefill_bytes(T, N, h_k, h_v, d_k, d_v, 2, x["state_in"] is not None)
+    traffic_key = {"chunked_coop": "chunk_coop", "chunked_split": "chunk_split"}.get(form)
+    rec = NCU_TRAFFIC.get(f"{traffic_key}@{name}") if traffic_key else None
+    traffic = None
+    if rec and source_hash(rec["files"]) == rec["sha256_16"]:
+        traffic = rec["bytes"]
+    out = {"form": form, "tokens": T, "sequences": N, "ms_per_call": ms,
+           "tok_s": T / (ms / 1e3), "tok_s_per_30_layers": T / (ms / 1e3) / 30,
+           "workspace_bytes": ws_n,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                        "traffic": traffic, "algorithmic_flop_per_launch": flop,
+                        "algorithmic_bytes_per_launch": nbytes,
+                        "hbm_gbs_at_algorithmic_bytes": nbytes / (ms / 1e3) / 1e9,
+                        "peak_source": f"{peaks['source']} bf16 dense (burst)"},
+           "l2": "flushed before each call (inputs are larger than L2 as well)"}
+    del x, o, st, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush):
@@ -841,17 +926,18 @@ def run_kernel_only(args):
         for _ in range(args.warmup + args.steps):
             gdn_decode_step(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"], o=o)
     else:
-        w = inputs.WORKLOADS[WORKLOAD]
+        name = WORKLOAD if args.kernel_only == "prefill" else args.kernel_only
+        w = inputs.WORKLOADS[name]
         d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"],
-                                w["dtype"], seed=w["seed"])
+                                w["dtype"], seed=w["seed"], state_std=w["state_std"])
         x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-        T = sum(w["lengths"])
-        n = gdn_prefill_workspace_size(1, T, w["h_k"], w["h_v"], w["d_k"], w["d_v"],
+        T, N = sum(w["lengths"]), len(w["lengths"])
+        n = gdn_prefill_workspace_size(N, T, w["h_k"], w["h_v"], w["d_k"], w["d_v"],
                                        torch.bfloat16, args.algo)
         ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
         for _ in range(args.warmup + args.steps):
             gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
-                        algo=args.algo, workspace=ws)
+                        state_in=x["state_in"], algo=args.algo, workspace=ws)
     torch.cuda.synchronize()
     assert gdn_stream_status() == "GDN_OK"
     print(f"kernel-only {args.kernel_only}: {args.warmup + args.steps} launches ok", flush=True)

@@ -247,7 +247,12 @@ size_t gdn_prefill_host_workspace_size(int64_t piece_tokens, int32_t h_k, int32_
  *
  * Set-up: the first call with a given device current looks up that device's
  * copy of the array (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Sharing: every call on a device uses the same array.
+ * stream capture.  The address is kept for the life of the process, so
+ * destroying the device's primary context after that first call (for example
+ * with cudaDeviceReset) is not supported: the kept address would be stale.
+ * The device error word that every entry point reports through
+ * gdn_stream_status is located the same way, once per device.
+ * Sharing: every call on a device uses the same array.
  * Nothing in it has to start at zero (each call writes what it later reads),
  * but calls whose kernels overlap on the GPU (other streams, other host
  * threads) race on it: order them, e.g. on one stream.  The array takes

@@ -21,20 +21,22 @@ def bench():
 
 def test_chunked_flops_from_product_shapes(bench):
     """Per chunk of C tokens: per key head the two Gram products, per value head
-    the WY products, the state-pass products and the triangular solve."""
+    the WY products and the state-pass products; the triangular solve apart."""
     C, h_k, h_v, d_k, d_v = 64, 16, 32, 128, 128
     mma = lambda m, n, k: 2 * m * n * k
     per_key = mma(C, C, d_k) + mma(C, C, d_k)                      # K K^T, Q K^T
     per_val = (mma(C, d_k, C) + mma(C, d_v, C)                    # W, U~
                + mma(C, d_v, C)                                    # P U
                + mma(C, d_v, d_k) + mma(C, d_v, d_k)               # W S^T, Q S^T
-               + mma(d_v, d_k, C)                                  # state update
-               + 2 * C ** 3 // 3)                                  # solve, C^3 / 3 MACs
+               + mma(d_v, d_k, C))                                 # state update
     want = (h_k * per_key + h_v * per_val) / C
     got = bench.chunked_flops_per_token(h_k, h_v, d_k, d_v)
     assert got == pytest.approx(want, rel=1e-12)
-    assert round(got) == 5_330_261                                  # the figure the roofline uses
-    assert got * 4096 == pytest.approx(21.83e9, rel=1e-3)
+    assert round(got) == 5_242_880                                  # the figure the roofline uses
+    assert got * 4096 == pytest.approx(21.47e9, rel=1e-3)
+    solve = bench.solve_flops_per_token(h_v)                        # C^3 / 3 MACs per chunk
+    assert solve == pytest.approx(h_v * (2 * C ** 3 // 3) / C, rel=1e-12)
+    assert round(got + solve) == 5_330_261
 
 
 def test_bytes_from_tensor_sizes(bench):

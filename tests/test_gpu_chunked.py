@@ -88,7 +88,7 @@ def test_prefill_t4096_full_oracle():
     o, st = run(d, algo="chunked_split")
     eo, es = full_errors(d, o, st)
     assert eo < TIGHT and es < TIGHT, (eo, es)
-    o2, st2 = run(d, algo="auto")  # AUTO picks the two kernels at this length
+    o2, st2 = run(d, algo="auto")  # AUTO takes the cooperative form at this length
     assert torch.equal(o2, o) and torch.equal(st2, st)
 
 

@@ -52,7 +52,7 @@ def test_too_many_chains_is_refused():
 
 
 def test_library_choice_takes_the_cooperative_form():
-    """algo='auto' on a sequence above the measured crossover (8,192 tokens) runs
+    """algo='auto' on a sequence above the measured crossover (4,096 tokens) runs
     the cooperative form through the workspace the size query reports."""
     x = inputs.make_prefill([9000], 2, 4, 128, 64, "bf16", seed=9, state_std=0.02)
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
@@ -68,7 +68,7 @@ def test_library_choice_takes_the_cooperative_form():
 
 
 def test_auto_mixes_the_cooperative_form_and_the_scan():
-    """AUTO on a batch averaging more than 8,192 tokens with one sequence below the
+    """AUTO on a batch averaging more than 4,096 tokens with one sequence below the
     scan crossover: the long sequence runs the cooperative form, the short one the
     token scan, in the same call; both against the fp64 oracle."""
     import numpy as np

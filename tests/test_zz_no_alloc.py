@@ -1,7 +1,15 @@
 """gdn_prefill_noalloc, the entry point that allocates nothing (its scratch is
 a fixed array the library holds in device memory), against gdn_prefill with a
-caller workspace: two calls in a row through the C ABI.  This file runs last
-and passes alone in a fresh process too."""
+caller workspace, through the C ABI.
+
+Both run the same deterministic two-kernel chunked evaluation on the same
+inputs, so their outputs must agree bit for bit; a mistake in handing the
+fixed array over as the workspace would show as a difference.  The calls run
+back to back on one stream with no synchronisation between them (two
+one-sequence calls, then a many-sequence one), so each call runs over the
+previous call's leftovers in the shared array, and the device's free memory
+and the torch allocator's counters are checked to be unchanged across them.
+This file runs last and passes alone in a fresh process too."""
 import ctypes
 
 import pytest
@@ -10,11 +18,8 @@ import torch
 from gated_deltanet_linear_recurrence_gb300 import (NOALLOC_SCRATCH_BYTES, _lib, gdn_prefill,
                                                     gdn_prefill_workspace_size,
                                                     gdn_stream_status, inputs)
-from tests.util import rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
-
-TIGHT = 8e-3  # the chunked tests' tolerance
 
 
 def dev(d):
@@ -33,13 +38,21 @@ def call_noalloc(lib, x, o, st, scale):
         ctypes.c_float(scale), torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_gdn_prefill_two_calls_in_a_row():
+def allocator_counters():
+    s = torch.cuda.memory_stats()
+    return (s.get("allocation.all.allocated", 0), s.get("segment.all.allocated", 0),
+            s.get("reserved_bytes.all.current", 0))
+
+
+def test_noalloc_matches_gdn_prefill_bitwise_back_to_back():
     lib = _lib.load()
-    cases = [  # the larger first, so the second call runs over the first call's leftovers
+    cases = [  # the largest first, so the later calls run over its leftovers
         (inputs.make_prefill([4096], 16, 32, 128, 128, "bf16", seed=31), 1.0),
+        (inputs.make_prefill([1000], 2, 4, 128, 64, "bf16", seed=34, state_std=0.05), 0.9),
         (inputs.make_prefill([300, 1, 777, 0, 64], 2, 4, 128, 64, "bf16", seed=32,
                              state_std=0.05), 0.7),
     ]
+    runs = []
     for d, scale in cases:
         x = dev(d)
         T, N = x["q"].shape[0], x["cu_seqlens"].numel() - 1
@@ -50,11 +63,26 @@ def test_noalloc_matches_gdn_prefill_two_calls_in_a_row():
                                     state_in=x["state_in"], scale=scale, algo="chunked_split")
         o = torch.full_like(o_ref, float("nan"))
         st = torch.full_like(st_ref, float("nan"))
+        runs.append((x, scale, o, st, o_ref, st_ref))
+    # one call first: the per-device set-up (the array's address) happens there
+    x, scale, o, st = runs[-1][:4]
+    assert call_noalloc(lib, x, o, st, scale) == _lib.GDN_OK
+    assert gdn_stream_status() == "GDN_OK"
+    for r in runs:
+        r[2].fill_(float("nan"))
+        r[3].fill_(float("nan"))
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    counters0 = allocator_counters()
+    for x, scale, o, st, _, _ in runs:  # back to back on one stream
         assert call_noalloc(lib, x, o, st, scale) == _lib.GDN_OK
-        assert gdn_stream_status() == "GDN_OK"
-        eo = rel_l2(to_np(o), to_np(o_ref))
-        es = rel_l2(to_np(st), to_np(st_ref))
-        assert eo < TIGHT and es < TIGHT, (eo, es)
+    assert gdn_stream_status() == "GDN_OK"
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, "device memory changed across the calls"
+    assert allocator_counters() == counters0, "the torch allocator was used"
+    for x, scale, o, st, o_ref, st_ref in runs:
+        assert torch.equal(o, o_ref)
+        assert torch.equal(st, st_ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
