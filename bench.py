@@ -283,9 +283,8 @@ def main():
     ap.add_argument("--no-long-prefill", action="store_true",
                     help="skip the 128K-token and ten-prompt varlen prefill timings")
     ap.add_argument("--sweep", action="store_true",
-                    help="time the token scan and the chunked prefill over sequence lengths "
-                         "(one sequence, 16 key / 32 value heads of 128, bf16) and print the "
-                         "crossover table as JSON lines")
+                    help="time every prefill form over sequence lengths for the shapes of the "
+                         "crossover table and print the timings and thresholds as JSON lines")
     ap.add_argument("--stream", action="store_true",
                     help="time the 128K-token prompt as one call and as streamed pieces "
                          "(gdn_prefill_streamed), with the workspace each needs, as JSON lines")
@@ -810,46 +809,132 @@ def bench_attention(torch, inputs, dev, stream, peaks, args, flush):
     return out
 
 
+def sweep_inputs(torch, dev, N, L, h_k, h_v, d_k, d_v, seed):
+    """Device-drawn inputs of the workloads' distributions for timing only (unit q,
+    k; v ~ N(0, 1); beta = sigmoid(N(0, 1)); g = -softplus(N(0, 1)); zero state):
+    nothing here is compared with the oracle."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    T = N * L
+
+    def unit(n_heads, d):
+        x = torch.randn((T, n_heads, d), generator=g, device=dev)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    x = {"q": unit(h_k, d_k), "k": unit(h_k, d_k),
+         "v": torch.randn((T, h_v, d_v), generator=g, device=dev).to(torch.bfloat16),
+         "beta": torch.sigmoid(torch.randn((T, h_v), generator=g, device=dev)),
+         "g": -torch.nn.functional.softplus(torch.randn((T, h_v), generator=g, device=dev)),
+         "cu_seqlens": torch.arange(0, T + 1, L, dtype=torch.int32, device=dev)}
+    return x
+
+
+SWEEP_LENGTHS = (8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192)
+SWEEP_MAX_TOKENS = 65536
+
+
+def sweep_thresholds(rows, forms):
+    """Per shape, from rows {L: {form: us}}: the smallest swept L from which the
+    faster of each pair stays faster at every longer L."""
+    Ls = sorted(rows)
+
+    def from_where(better, worse):
+        start = None
+        for L in Ls:
+            r = rows[L]
+            if better not in r or worse not in r:
+                continue
+            if r[better] < r[worse]:
+                if start is None:
+                    start = L
+            else:
+                start = None
+        return start
+
+    chunked = [f for f in ("chunked_fused", "chunked_split") if f in forms]
+    best = {L: min(rows[L][f] for f in chunked if f in rows[L]) for L in Ls
+            if any(f in rows[L] for f in chunked)}
+    scan_below = None
+    for L in Ls:
+        if L not in best or "scan" not in rows[L]:
+            continue
+        if best[L] < rows[L]["scan"]:
+            if scan_below is None:
+                scan_below = L
+        else:
+            scan_below = None
+    split_from = from_where("chunked_split", "chunked_fused") if "chunked_fused" in forms else 0
+    coop_from = from_where("chunked_coop", "chunked_split") if "chunked_coop" in forms else None
+    return {"scan_below": scan_below, "split_from_avg": split_from, "coop_from_avg": coop_from}
+
+
 def run_sweep(args):
-    """Scan vs chunked prefill time over sequence lengths (L2 flushed before each call)."""
+    """Every prefill form timed over sequence lengths for each shape of the
+    crossover table (d_k 64 / 128, d_v 32 / 64 / 128, 4 / 32 value heads with two
+    per key head, 1 / 4 / 16 sequences of equal length), L2 flushed before each
+    call; prints one JSON line per (shape, length) and one per shape with the
+    thresholds the table takes."""
     import torch
-    from gated_deltanet_linear_recurrence_gb300 import gdn_prefill, gdn_stream_status, inputs
+    from gated_deltanet_linear_recurrence_gb300 import (_lib, gdn_prefill, gdn_prefill_workspace_size,
+                                                        gdn_stream_status)
 
     dev = torch.device("cuda", 0)
     flush = make_flush(torch, dev, torch.cuda.get_device_properties(dev).L2_cache_size)
-    lengths = [8, 16, 32, 64, 128, 256, 384, 512, 768, 1024, 2048, 4096, 8192, 16384, 65536,
-               131072]
-    rows = []
-    for T in lengths:
-        d = inputs.make_prefill([T], 16, 32, 128, 128, "bf16", seed=T)
-        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-        res = {"T": T}
-        # chunked = two kernels through a workspace; chunked_fused = one kernel, none
-        for name, algo in (("scan", "scan"), ("chunked", "chunked_split"),
-                           ("chunked_fused", "chunked_fused")):
-            reps = 3 if (algo == "scan" and T >= 16384) else 7
-            ts = []
-            for i in range(reps + 2):
-                flush()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"],
-                            algo=algo)
-                b.record()
-                torch.cuda.synchronize()
-                if i >= 2:
-                    ts.append(a.elapsed_time(b) * 1e3)
-            assert gdn_stream_status() == "GDN_OK"
-            res[name + "_us"] = statistics.median(ts)
-        res["chunked_tok_s"] = T / (res["chunked_us"] / 1e6)
-        res["chunked_fused_tok_s"] = T / (res["chunked_fused_us"] / 1e6)
-        res["scan_tok_s"] = T / (res["scan_us"] / 1e6)
-        rows.append(res)
-        print(json.dumps(res), flush=True)
-    cross = next((r["T"] for r in rows
-                  if min(r["chunked_us"], r["chunked_fused_us"]) < r["scan_us"]), None)
-    split = next((r["T"] for r in rows if r["chunked_us"] < r["chunked_fused_us"]), None)
-    print(json.dumps({"crossover_tokens": cross, "split_from_tokens": split}), flush=True)
+    lib = _lib.load()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ws = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    for d_k in (128, 64):
+        for d_v in (128, 64, 32):
+            for h_v in (32, 4):
+                for N in (1, 4, 16):
+                    h_k = h_v // 2
+                    forms = ["scan", "chunked_split"]
+                    if d_k == 128:
+                        forms.insert(1, "chunked_fused")
+                    coop_ok = d_v % 64 == 0 and N * h_v * (d_v // 64) <= sms * 2 // 3
+                    if coop_ok:
+                        forms.append("chunked_coop")
+                    rows, scan_on = {}, True
+                    for L in SWEEP_LENGTHS:
+                        if N * L > SWEEP_MAX_TOKENS:
+                            break
+                        x = sweep_inputs(torch, dev, N, L, h_k, h_v, d_k, d_v, seed=L + N)
+                        T = N * L
+                        o = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
+                        st = torch.empty((N, h_v, d_v, d_k), dtype=torch.float32, device=dev)
+                        res = {}
+                        for f in forms:
+                            if f == "scan" and not scan_on:
+                                continue
+                            need = gdn_prefill_workspace_size(N, T, h_k, h_v, d_k, d_v,
+                                                              torch.bfloat16, f)
+                            assert need <= ws.numel()
+                            ts = []
+                            for i in range(6):
+                                flush()
+                                a = torch.cuda.Event(enable_timing=True)
+                                b = torch.cuda.Event(enable_timing=True)
+                                a.record()
+                                gdn_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                            x["cu_seqlens"], state_out=st, o=o, algo=f,
+                                            workspace=ws if need else None)
+                                b.record()
+                                b.synchronize()
+                                if i >= 1:
+                                    ts.append(a.elapsed_time(b) * 1e3)
+                            assert gdn_stream_status() == "GDN_OK"
+                            res[f] = statistics.median(ts)
+                        chunk_best = min(v for k, v in res.items() if k != "scan")
+                        if "scan" in res and res["scan"] > 4 * chunk_best:
+                            scan_on = False  # the scan only falls further behind
+                        rows[L] = res
+                        print(json.dumps({"d_k": d_k, "d_v": d_v, "h_v": h_v, "N": N, "L": L,
+                                          "us": {k: round(v, 2) for k, v in res.items()}}),
+                              flush=True)
+                        del x, o, st
+                    th = sweep_thresholds(rows, forms)
+                    print(json.dumps({"shape": {"d_k": d_k, "d_v": d_v, "h_v": h_v, "N": N},
+                                      "thresholds": th}), flush=True)
 
 
 def run_stream(args):

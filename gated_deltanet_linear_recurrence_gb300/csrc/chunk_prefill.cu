@@ -575,16 +575,24 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
 
 }  // namespace
 
+// Shapes the chunked evaluation covers: bf16 operands, d_v a multiple of 32,
+// d_k 128 or 64 (the two-kernel and cooperative forms read Q and K as 3-D
+// tiles whose columns past d_k arrive as zeros, so d_k = 64 runs as 128 with
+// zero padding); the fused kernel needs d_k = 128.
 bool chunked_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
-  return dtype == kBF16 && d_k == kDK && d_v >= kDVS && d_v % kDVS == 0 && h_k > 0 &&
-         h_v % h_k == 0;
+  return dtype == kBF16 && (d_k == kDK || d_k == kDK / 2) && d_v >= kDVS && d_v % kDVS == 0 &&
+         h_k > 0 && h_v % h_k == 0;
+}
+
+bool fused_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
+  return chunked_supports(h_k, h_v, d_k, d_v, dtype) && d_k == kDK;
 }
 
 size_t chunked_workspace_bytes(int32_t, int64_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
-  if (!chunked_supports(a.h_k, a.h_v, a.d_k, a.d_v, a.dtype)) return cudaErrorNotSupported;
+  if (!fused_supports(a.h_k, a.h_v, a.d_k, a.d_v, a.dtype)) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   const uint64_t rows = a.total_tokens > 0 ? (uint64_t)a.total_tokens : 1;
   // With no tokens every sequence is empty and no TMA is issued; the maps still

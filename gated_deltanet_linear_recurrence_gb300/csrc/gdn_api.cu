@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "gdn.h"
@@ -42,38 +43,102 @@ gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
   return GDN_OK;
 }
 
-// Crossover: the sequence length from which the chunked evaluation is faster
-// than the token scan.  Measured on GB300 (bench.py --sweep: one sequence,
-// 16 key / 32 value heads of 128, bf16; L2 flushed before each call): the
-// fused chunked kernel ties the scan at 8 tokens (13.0 vs 12.9 us) and is
-// faster from 16 tokens up (13.0 vs 19.1 us), so sequences shorter than 16
-// tokens use the scan.  Shapes the chunked kernels do not cover (d_k != 128,
-// d_v not a multiple of 32, fp32 inputs) always scan.
-constexpr int32_t kCrossoverTokens = 16;
+// Which evaluation is fastest, by shape: a table measured on GB300 with
+// bench.py --sweep (N sequences of equal length L, bf16, L2 flushed before each
+// call; every form timed at every L; profiles/crossover_table.md).  Per entry:
+//   scan_below      sequences shorter than this take the token scan (per
+//                   sequence, so one call can mix the two);
+//   split_from_avg  the two-kernel form instead of the fused kernel from this
+//                   average length (when the caller's workspace holds it);
+//   coop_from_avg   the cooperative form instead of the two kernels from this
+//                   average length (when its chains fit: coop_supported).
+// A shape takes the entry with the same d_k that is nearest in d_v, then in
+// log2(h_v), then in log2(N).  fp32 inputs, and shapes no chunked form covers,
+// always scan.
+struct FormThresholds {
+  int32_t scan_below;
+  int64_t split_from_avg, coop_from_avg;
+};
+struct CrossoverEntry {
+  int32_t d_k, d_v, h_v, n;
+  FormThresholds t;
+};
+constexpr int64_t kNever = INT64_MAX;
+constexpr CrossoverEntry kCrossover[] = {
+    // d_k, d_v, h_v, N: {scan below, two kernels from, cooperative from}
+    {128, 128, 32, 1, {16, 256, 4096}},
+    {128, 128, 32, 4, {16, 8, kNever}},
+    {128, 128, 32, 16, {8, 8, kNever}},
+    {128, 128, 4, 1, {16, 256, kNever}},
+    {128, 128, 4, 4, {16, 512, kNever}},
+    {128, 128, 4, 16, {32, 128, kNever}},
+    {128, 64, 32, 1, {16, 256, 8192}},
+    {128, 64, 32, 4, {16, 128, kNever}},
+    {128, 64, 32, 16, {16, 8, kNever}},
+    {128, 64, 4, 1, {16, 256, kNever}},
+    {128, 64, 4, 4, {16, 512, kNever}},
+    {128, 64, 4, 16, {8, 512, kNever}},
+    {128, 32, 32, 1, {16, 256, kNever}},
+    {128, 32, 32, 4, {16, 1024, kNever}},
+    {128, 32, 32, 16, {16, 512, kNever}},
+    {128, 32, 4, 1, {16, 256, kNever}},
+    {128, 32, 4, 4, {16, 512, kNever}},
+    {128, 32, 4, 16, {16, 512, kNever}},
+    {64, 128, 32, 1, {16, 0, 4096}},
+    {64, 128, 32, 4, {32, 0, kNever}},
+    {64, 128, 32, 16, {16, 0, kNever}},
+    {64, 128, 4, 1, {32, 0, kNever}},
+    {64, 128, 4, 4, {32, 0, kNever}},
+    {64, 128, 4, 16, {32, 0, kNever}},
+    {64, 64, 32, 1, {16, 0, 4096}},
+    {64, 64, 32, 4, {32, 0, kNever}},
+    {64, 64, 32, 16, {32, 0, kNever}},
+    {64, 64, 4, 1, {32, 0, kNever}},
+    {64, 64, 4, 4, {32, 0, kNever}},
+    {64, 64, 4, 16, {32, 0, kNever}},
+    {64, 32, 32, 1, {16, 0, kNever}},
+    {64, 32, 32, 4, {32, 0, kNever}},
+    {64, 32, 32, 16, {64, 0, kNever}},
+    {64, 32, 4, 1, {16, 0, kNever}},
+    {64, 32, 4, 4, {32, 0, kNever}},
+    {64, 32, 4, 16, {32, 0, kNever}},
+};
 
-// Fused vs two-kernel chunked evaluation.  Same sweep: the fused kernel is
-// faster up to 128 tokens (17.1 vs 20.1 us), the two kernels from 256 tokens
-// (23.2 vs 25.2 us; 3.20 vs 7.83 ms at 128K tokens).  GDN_ALGO_AUTO and
-// GDN_ALGO_CHUNKED use the two kernels when the sequences average at least
-// this many tokens and the caller's workspace is large enough.
-constexpr int64_t kSplitMinAvgTokens = 256;
-
-// Two kernels vs one cooperative kernel (prepare and chain overlapped in one
-// grid).  Same sweep, one sequence: the two kernels are faster at 2,048 tokens
-// (63.5 vs 67.6 us), about even at 3,072 (90.1 vs 88.6 us), the cooperative
-// kernel faster from 4,096 (110.5 vs 104.4 us with the current state pass;
-// 395.6 vs 344.9 us at 16K, 3.08 vs 2.58 ms at 128K).  GDN_ALGO_AUTO and
-// GDN_ALGO_CHUNKED use it from this average length when its chains fit
-// (coop_supported) and the workspace holds its flags.
-constexpr int64_t kCoopMinAvgTokens = 4096;
-
-bool split_preferred(int32_t num_seqs, int64_t total_tokens) {
-  return num_seqs > 0 && total_tokens >= kSplitMinAvgTokens * num_seqs;
+// The sequences average at least `threshold` tokens (no overflow for kNever).
+bool avg_at_least(int64_t total_tokens, int32_t num_seqs, int64_t threshold) {
+  return num_seqs > 0 && total_tokens / num_seqs >= threshold;
 }
 
-int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype) {
+int log2_floor(int64_t x) {
+  int r = 0;
+  while (x > 1) {
+    x >>= 1;
+    ++r;
+  }
+  return r;
+}
+
+FormThresholds thresholds_for(int32_t h_v, int32_t d_k, int32_t d_v, int32_t num_seqs) {
+  const CrossoverEntry* best = nullptr;
+  int64_t best_key = INT64_MAX;
+  for (const CrossoverEntry& e : kCrossover) {
+    const int64_t dk = e.d_k == d_k ? 0 : 1;
+    const int64_t dv = e.d_v > d_v ? e.d_v - d_v : d_v - e.d_v;
+    const int64_t dh = std::abs(log2_floor(e.h_v) - log2_floor(h_v));
+    const int64_t dn = std::abs(log2_floor(e.n) - log2_floor(num_seqs > 0 ? num_seqs : 1));
+    const int64_t key = ((dk * 1024 + dv) * 64 + dh) * 64 + dn;
+    if (key < best_key) {
+      best_key = key;
+      best = &e;
+    }
+  }
+  return best->t;
+}
+
+int32_t crossover_for(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype,
+                      int32_t num_seqs = 1) {
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return INT32_MAX;
-  return kCrossoverTokens;
+  return thresholds_for(h_v, d_k, d_v, num_seqs).scan_below;
 }
 
 constexpr int32_t kAttnHeadDim = 256;
@@ -140,10 +205,15 @@ Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32
     return r;
   };
   const bool chunk_ok = gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype);
+  // the fused kernel covers d_k = 128 without the normalisation option
+  const bool fused_ok = gdn::fused_supports(h_k, h_v, d_k, d_v, dtype) && !qk_norm;
   const bool chunk_only = algo == GDN_ALGO_CHUNKED || algo == GDN_ALGO_CHUNKED_FUSED ||
                           algo == GDN_ALGO_CHUNKED_SPLIT || algo == GDN_ALGO_CHUNKED_COOP;
   if (chunk_only && !chunk_ok)
     return fail(dtype == GDN_F32 ? GDN_ERR_UNSUPPORTED_DTYPE : GDN_ERR_UNSUPPORTED_SHAPE);
+  if (algo == GDN_ALGO_CHUNKED_FUSED && !gdn::fused_supports(h_k, h_v, d_k, d_v, dtype))
+    return fail(GDN_ERR_UNSUPPORTED_SHAPE);
+  const FormThresholds th = thresholds_for(h_v, d_k, d_v, num_seqs);
   // Scan for sequences shorter than min_chunk_len, chunked for the rest.  With
   // one sequence its length is total_tokens, so only the kernel with work runs.
   if (algo == GDN_ALGO_SCAN) {
@@ -153,14 +223,14 @@ Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32
     r.run_scan = false;
     r.run_chunk = true;
   } else {
-    r.min_chunk_len = crossover_for(h_k, h_v, d_k, d_v, dtype);
+    r.min_chunk_len = chunk_ok ? th.scan_below : INT32_MAX;
     r.run_chunk = chunk_ok && total_tokens >= r.min_chunk_len;
     r.run_scan = !(num_seqs == 1 && r.run_chunk);
   }
   // The chunked evaluation runs as one fused kernel, as two kernels meeting in
   // the caller's workspace (forced by GDN_ALGO_CHUNKED_SPLIT; otherwise when the
-  // sequences are long enough and the workspace is large enough), or as one
-  // cooperative kernel through the workspace.
+  // sequences are long enough, or the fused kernel does not cover the call, and
+  // the workspace is large enough), or as one cooperative kernel through it.
   if (r.run_chunk && algo == GDN_ALGO_CHUNKED_COOP) {
     if (!have_ws) return fail(GDN_ERR_NULL_POINTER);
     if (!ws_aligned) return fail(GDN_ERR_MISALIGNED);
@@ -177,15 +247,17 @@ Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32
     }
     if (have_ws && !ws_aligned) return fail(GDN_ERR_MISALIGNED);
     r.split = have_ws && workspace_bytes >= need &&
-              (algo == GDN_ALGO_CHUNKED_SPLIT || qk_norm || split_preferred(num_seqs, total_tokens));
-    if (qk_norm && !r.split) {  // no room for the two kernels: the token scan takes everything
+              (algo == GDN_ALGO_CHUNKED_SPLIT || !fused_ok ||
+               avg_at_least(total_tokens, num_seqs, th.split_from_avg));
+    if (!fused_ok && !r.split) {  // no room for the two kernels: the token scan takes everything
       if (algo == GDN_ALGO_CHUNKED) return fail(GDN_ERR_WORKSPACE_TOO_SMALL);
       r.run_chunk = false;
       r.run_scan = true;
       r.min_chunk_len = INT32_MAX;
     }
   }
-  if (r.split && algo != GDN_ALGO_CHUNKED_SPLIT && total_tokens >= kCoopMinAvgTokens * num_seqs &&
+  if (r.split && algo != GDN_ALGO_CHUNKED_SPLIT &&
+      avg_at_least(total_tokens, num_seqs, th.coop_from_avg) &&
       workspace_bytes >= gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v) && sms > 0 &&
       gdn::coop_supported(num_seqs, h_v, d_v, sms)) {
     r.coop = true;
@@ -228,8 +300,12 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
   if (algo == GDN_ALGO_SCAN || algo == GDN_ALGO_CHUNKED_FUSED) return 0;
   if (!gdn::chunked_supports(h_k, h_v, d_k, d_v, dtype)) return 0;
   if (algo == GDN_ALGO_CHUNKED_SPLIT) return gdn::split_workspace_bytes(num_seqs, total_tokens, h_v);
-  if (algo != GDN_ALGO_CHUNKED_COOP && !split_preferred(num_seqs, total_tokens)) return 0;
-  // AUTO and CHUNKED: room for the cooperative form (the two-kernel form plus flags)
+  // AUTO and CHUNKED: none while the fused kernel is the faster form (and covers
+  // the shape), else room for the cooperative form (the two-kernel form plus flags)
+  const FormThresholds th = thresholds_for(h_v, d_k, d_v, num_seqs);
+  if (algo != GDN_ALGO_CHUNKED_COOP && gdn::fused_supports(h_k, h_v, d_k, d_v, dtype) &&
+      !avg_at_least(total_tokens, num_seqs, th.split_from_avg))
+    return 0;
   return gdn::coop_workspace_bytes(num_seqs, total_tokens, h_v);
 }
 

@@ -107,6 +107,7 @@ cudaError_t launch_chunked(const PrefillArgs& a, cudaStream_t stream);
 size_t chunked_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_k, int32_t h_v,
                                int32_t d_k, int32_t d_v);
 bool chunked_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype);
+bool fused_supports(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v, int dtype);
 // Two-kernel chunked prefill (prepare + chain) through a caller workspace.
 size_t split_workspace_bytes(int32_t num_seqs, int64_t total_tokens, int32_t h_v);
 cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream);

