@@ -44,8 +44,11 @@ gdn_status check_heads(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v) {
 }
 
 // Which evaluation is fastest, by shape: a table measured on GB300 with
-// bench.py --sweep (N sequences of equal length L, bf16, L2 flushed before each
-// call; every form timed at every L; profiles/crossover_table.md).  Per entry:
+// bench.py --sweep (N sequences of equal length L = 8 ... 8192, at most 65,536
+// tokens a call, bf16, L2 flushed before each call, every form timed at every
+// L; a threshold is the smallest swept L from which the faster form stays
+// faster, so it is known to a factor of two and flips between neighbouring
+// lengths where two forms time within noise of each other).  Per entry:
 //   scan_below      sequences shorter than this take the token scan (per
 //                   sequence, so one call can mix the two);
 //   split_from_avg  the two-kernel form instead of the fused kernel from this
@@ -69,18 +72,18 @@ constexpr CrossoverEntry kCrossover[] = {
     {128, 128, 32, 1, {16, 256, 4096}},
     {128, 128, 32, 4, {16, 8, kNever}},
     {128, 128, 32, 16, {8, 8, kNever}},
-    {128, 128, 4, 1, {16, 256, kNever}},
+    {128, 128, 4, 1, {16, 512, kNever}},
     {128, 128, 4, 4, {16, 512, kNever}},
-    {128, 128, 4, 16, {32, 128, kNever}},
+    {128, 128, 4, 16, {16, 128, kNever}},
     {128, 64, 32, 1, {16, 256, 8192}},
-    {128, 64, 32, 4, {16, 128, kNever}},
+    {128, 64, 32, 4, {32, 128, kNever}},
     {128, 64, 32, 16, {16, 8, kNever}},
     {128, 64, 4, 1, {16, 256, kNever}},
-    {128, 64, 4, 4, {16, 512, kNever}},
-    {128, 64, 4, 16, {8, 512, kNever}},
+    {128, 64, 4, 4, {8, 512, kNever}},
+    {128, 64, 4, 16, {16, 512, kNever}},
     {128, 32, 32, 1, {16, 256, kNever}},
     {128, 32, 32, 4, {16, 1024, kNever}},
-    {128, 32, 32, 16, {16, 512, kNever}},
+    {128, 32, 32, 16, {32, 256, kNever}},
     {128, 32, 4, 1, {16, 256, kNever}},
     {128, 32, 4, 4, {16, 512, kNever}},
     {128, 32, 4, 16, {16, 512, kNever}},
@@ -90,16 +93,16 @@ constexpr CrossoverEntry kCrossover[] = {
     {64, 128, 4, 1, {32, 0, kNever}},
     {64, 128, 4, 4, {32, 0, kNever}},
     {64, 128, 4, 16, {32, 0, kNever}},
-    {64, 64, 32, 1, {16, 0, 4096}},
+    {64, 64, 32, 1, {16, 0, 8192}},
     {64, 64, 32, 4, {32, 0, kNever}},
     {64, 64, 32, 16, {32, 0, kNever}},
-    {64, 64, 4, 1, {32, 0, kNever}},
+    {64, 64, 4, 1, {16, 0, kNever}},
     {64, 64, 4, 4, {32, 0, kNever}},
     {64, 64, 4, 16, {32, 0, kNever}},
-    {64, 32, 32, 1, {16, 0, kNever}},
+    {64, 32, 32, 1, {32, 0, kNever}},
     {64, 32, 32, 4, {32, 0, kNever}},
     {64, 32, 32, 16, {64, 0, kNever}},
-    {64, 32, 4, 1, {16, 0, kNever}},
+    {64, 32, 4, 1, {32, 0, kNever}},
     {64, 32, 4, 4, {32, 0, kNever}},
     {64, 32, 4, 16, {32, 0, kNever}},
 };
@@ -223,8 +226,12 @@ Route route_prefill(gdn_algo algo, int32_t num_seqs, int64_t total_tokens, int32
     r.run_scan = false;
     r.run_chunk = true;
   } else {
-    r.min_chunk_len = chunk_ok ? th.scan_below : INT32_MAX;
-    r.run_chunk = chunk_ok && total_tokens >= r.min_chunk_len;
+    // The table was measured on batches of equal lengths, so a batch whose
+    // sequences average fewer than scan_below tokens goes to the scan whole
+    // (no chunked launch with nothing to do); otherwise sequences shorter than
+    // scan_below still take the scan, beside the chunked kernels.
+    r.run_chunk = chunk_ok && avg_at_least(total_tokens, num_seqs, th.scan_below);
+    r.min_chunk_len = r.run_chunk ? th.scan_below : INT32_MAX;
     r.run_scan = !(num_seqs == 1 && r.run_chunk);
   }
   // The chunked evaluation runs as one fused kernel, as two kernels meeting in
