@@ -86,7 +86,7 @@ struct SplitParams {
   const int32_t* cu;
   int32_t num_seqs;
   int64_t total_tokens;
-  int32_t h_k, h_v, d_k, d_v;  // d_k 64 or 128: Q, K arrive zero-padded to 128 columns
+  int32_t h_k, h_v, d_v;  // (d_k: the kernels' template parameter DKP)
   float scale;
   int32_t min_len;
   int qk_norm;          // q and k divided by their L2 norm (+1e-6 under the root)
@@ -233,14 +233,17 @@ __device__ __forceinline__ bool item_chunk(const SplitParams& p, int64_t item, i
   return true;
 }
 
-// Copy the 64-column half kb of key head hk's Q or K rows y .. y + 63.  For
-// d_k = 128 the map is 2-D ([rows][h_k * 128], measured ~5 % faster per call
-// than the 3-D form at 4,096 tokens); for d_k = 64 it is 3-D ([rows][h_k][64])
-// and the half at column 64 lies past the head's columns, so it arrives as
-// zeros: the kernels see every key head zero-padded to 128 columns.
-__device__ __forceinline__ void kq_load(void* dst, const CUtensorMap* map, int32_t d_k, int hk,
-                                        int kb, int32_t y, uint64_t* bar) {
-  if (d_k == kDK)
+// Copy the 64-column half kb of key head hk's Q or K rows y .. y + 63.  The
+// kernels below are compiled once per key dimension DKP: for DKP = 128 the map
+// is 2-D ([rows][h_k * 128]); for DKP = 64 it is 3-D ([rows][h_k][64]) and the
+// half at column 64 lies past the head's columns, so it arrives as zeros: the
+// kernels see every key head zero-padded to 128 columns.  (A single build with
+// a run-time choice measured ~5 % slower at 4,096 tokens than the 128-only code.)
+template <int DKP>
+__device__ __forceinline__ void kq_load(void* dst, const CUtensorMap* map, int hk, int kb,
+                                        int32_t y, uint64_t* bar) {
+  static_assert(DKP == kDK || DKP == kDK / 2, "key dimension 128 or 64");
+  if constexpr (DKP == kDK)
     tc::tma_load_2d(dst, map, hk * kDK + 64 * kb, y, bar);
   else
     tc::tma_load_3d(dst, map, 64 * kb, hk, y, bar);
@@ -248,6 +251,7 @@ __device__ __forceinline__ void kq_load(void* dst, const CUtensorMap* map, int32
 
 // Thread 0 of a prepare item issues the copies of its chunk's Q and K rows
 // (key head of value head h) into the item's shared memory; bars[0] counts them.
+template <int DKP>
 __device__ __forceinline__ void prepare_loads(const SplitParams& p, const CUtensorMap* tm_q,
                                               const CUtensorMap* tm_k, uint8_t* smem,
                                               uint64_t* bars, int64_t item, int n, int c) {
@@ -257,8 +261,8 @@ __device__ __forceinline__ void prepare_loads(const SplitParams& p, const CUtens
   tc::mbar_arrive_expect_tx(bars, 32768);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb) {
-    kq_load(smem + PP_KQ + kb * 16384, tm_q, p.d_k, hk, kb, y, bars);
-    kq_load(smem + PP_KQ + kb * 16384 + 8192, tm_k, p.d_k, hk, kb, y, bars);
+    kq_load<DKP>(smem + PP_KQ + kb * 16384, tm_q, hk, kb, y, bars);
+    kq_load<DKP>(smem + PP_KQ + kb * 16384 + 8192, tm_k, hk, kb, y, bars);
   }
 }
 
@@ -548,6 +552,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
   return ok;
 }
 
+template <int DKP>
 __global__ void __launch_bounds__(kPrepThreads, 4)
     chunk_prepare_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   if (pt == 0) {
     for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
     tc::fence_mbar_init();
-    prepare_loads(p, &tm_q, &tm_k, smem, bars, item, n, c);
+    prepare_loads<DKP>(p, &tm_q, &tm_k, smem, bars, item, n, c);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -659,7 +664,7 @@ __device__ __forceinline__ bool wait_item_flag(const int* flag,
 // on ChainCfg::kThreads threads: EW epilogue warps, a producer warp and an MMA
 // warp.  With item_flags, a chunk's package is copied only once its flag is
 // set (its prepare item runs in another CTA of the same cooperative grid).
-template <int DVS, int NSTG, int EW>
+template <int DVS, int NSTG, int EW, int DKP>
 __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, uint8_t* smem, int n, int h,
                                           int s, int tid, const int* item_flags) {
@@ -740,8 +745,8 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         tc::mbar_arrive_expect_tx(fb, CF::kMainTx);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          kq_load(dst + kb * kHalf + SC_Q, tm_q, p.d_k, hk, kb, y, fb);
-          kq_load(dst + kb * kHalf + SC_K, tm_k, p.d_k, hk, kb, y, fb);
+          kq_load<DKP>(dst + kb * kHalf + SC_Q, tm_q, hk, kb, y, fb);
+          kq_load<DKP>(dst + kb * kHalf + SC_K, tm_k, hk, kb, y, fb);
           bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
         }
         bulk_g2s(dst + SC_U, pkg + kPkgU + s * CF::NB * kPkgUSlice, CF::NB * kPkgUSlice, fb);
@@ -918,13 +923,13 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       float sc[32 * BPW];
 #pragma unroll
       for (int i = 0; i < 32 * BPW; ++i)
-        sc[i] = p.state_in && jrow < p.d_k ? p.state_in[(srow0 + 32 * b0 + i) * p.d_k + jrow]
-                                           : 0.f;  // key columns past d_k stay zero
+        sc[i] = p.state_in && jrow < DKP ? p.state_in[(srow0 + 32 * b0 + i) * DKP + jrow]
+                                         : 0.f;  // key columns past d_k stay zero
       if (nchunks == 0) {
-        if (jrow < p.d_k)
+        if (jrow < DKP)
 #pragma unroll
           for (int i = 0; i < 32 * BPW; ++i)
-            p.state_out[(srow0 + 32 * b0 + i) * p.d_k + jrow] = sc[i];
+            p.state_out[(srow0 + 32 * b0 + i) * DKP + jrow] = sc[i];
       } else {
         preload(0);
         stage_state(sc, 0);
@@ -967,10 +972,10 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
         tc::tmem_ld32(tmem + lane_base + CF::TC_S + 32 * (b0 + b),
                       *reinterpret_cast<float(*)[32]>(sc + 32 * b));
       if (c == nchunks - 1) {
-        if (jrow < p.d_k)
+        if (jrow < DKP)
 #pragma unroll
           for (int i = 0; i < 32 * BPW; ++i)
-            p.state_out[(srow0 + 32 * b0 + i) * p.d_k + jrow] = sc[i];
+            p.state_out[(srow0 + 32 * b0 + i) * DKP + jrow] = sc[i];
       } else {
         stage_state(sc, c + 1);
       }
@@ -994,7 +999,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
 using SplitChain = ChainCfg<kDVS, 3, 4>;
 using SplitChain64 = ChainCfg<64, 3, 8>;
 
-template <class CF>
+template <class CF, int DKP>
 __global__ void __launch_bounds__(CF::kThreads, 1)
     chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const SplitParams p) {
@@ -1010,7 +1015,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     wait_prerequisites();  // the plan kernel's order
     n = p.order[blockIdx.x / (ns * p.h_v)];
   }
-  chain_run<kRows, CF::kStages, CF::kEW>(p, &tm_q, &tm_k, smem, n, h, s, threadIdx.x, nullptr);
+  chain_run<kRows, CF::kStages, CF::kEW, DKP>(p, &tm_q, &tm_k, smem, n, h, s, threadIdx.x,
+                                              nullptr);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1086,6 +1092,7 @@ constexpr uint32_t kSlotStaggerNs = 2000;
 // r takes s x n_prep + r, so the first chunks spread over the SMs); later items
 // come from a counter shared by all n_slots slots (flags[max_items], zero at
 // launch), in increasing order, i.e. chunk by chunk.
+template <int DKP>
 __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CUtensorMap* tm_q,
                                                   const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                   uint8_t* smem, int pt, int* flags, uint32_t bA,
@@ -1114,7 +1121,7 @@ __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CU
     const int64_t item = *next;
     int n, c;
     if (!ok || item >= p.max_items || !item_chunk(p, item, n, c)) break;  // past the last chunk
-    if (pt == 0) prepare_loads(p, tm_q, tm_k, smem, bars, item, n, c);
+    if (pt == 0) prepare_loads<DKP>(p, tm_q, tm_k, smem, bars, item, n, c);
     ok = prepare_item(p, tm_v, smem, tmem, bars, k, pt, item, n, c, bA, bG);
     // Every thread's package stores are visible device-wide before the flag;
     // the slot's shared memory and TMEM are free for the next item.
@@ -1134,6 +1141,7 @@ __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CU
   if (pt < 32) tc::tmem_dealloc(tmem, kPrepTmemCols);
 }
 
+template <int DKP>
 __global__ void __launch_bounds__(kCoopThreads, 1)
     chunk_coop_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -1149,7 +1157,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     const int s = blockIdx.x % ns;
     const int h = (blockIdx.x / ns) % p.h_v;
     const int n = blockIdx.x / (ns * p.h_v);
-    chain_run<kRows, CoopChain::kStages, CoopChain::kEW>(p, &tm_q, &tm_k, smem, n, h, s,
+    chain_run<kRows, CoopChain::kStages, CoopChain::kEW, DKP>(p, &tm_q, &tm_k, smem, n, h, s,
                                                          threadIdx.x, flags);
     return;
   }
@@ -1158,7 +1166,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
   uint8_t* sm = smem + slot * kPrepSlotBytes;
   // named barriers 1 + 2 slot (the slot's 128 threads) and 2 + 2 slot (its first 64)
   const int n_prep = (int)gridDim.x - n_chain;
-  coop_prepare_slot(p, &tm_q, &tm_k, &tm_v, sm, pt, flags, 1u + 2u * slot, 2u + 2u * slot, slot,
+  coop_prepare_slot<DKP>(p, &tm_q, &tm_k, &tm_v, sm, pt, flags, 1u + 2u * slot, 2u + 2u * slot,
+                         slot,
                     slot * n_prep + ((int)blockIdx.x - n_chain), n_prep * kCoopSlots);
 }
 
@@ -1210,7 +1219,6 @@ bool split_setup(const PrefillArgs& a, void* workspace, CUtensorMap& mq, CUtenso
   p.total_tokens = a.total_tokens;
   p.h_k = a.h_k;
   p.h_v = a.h_v;
-  p.d_k = a.d_k;
   p.d_v = a.d_v;
   p.scale = a.scale;
   p.min_len = a.min_chunk_len;
@@ -1224,26 +1232,23 @@ bool split_setup(const PrefillArgs& a, void* workspace, CUtensorMap& mq, CUtenso
   return true;
 }
 
-cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  if (!coop_supported(a.num_seqs, a.h_v, a.d_v, sms)) return cudaErrorNotSupported;
+namespace {
+
+template <int DKP>
+cudaError_t launch_coop_dk(const PrefillArgs& a, void* workspace, cudaStream_t stream, int sms) {
   CUtensorMap mq, mk, mv;
   SplitParams p;
   if (!split_setup(a, workspace, mq, mk, mv, p)) return cudaErrorInvalidValue;
   if (p.max_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   static PerDeviceOnce attrs;
-  e = attrs.run([] {
-    return cudaFuncSetAttribute(chunk_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = attrs.run([] {
+    return cudaFuncSetAttribute(chunk_coop_kernel<DKP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kCoopSmem);
   });
   if (e != cudaSuccess) return e;
   int resident = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, chunk_coop_kernel, kCoopThreads,
-                                                    kCoopSmem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, chunk_coop_kernel<DKP>,
+                                                    kCoopThreads, kCoopSmem);
   if (e != cudaSuccess) return e;
   if (resident < 1) return cudaErrorNotSupported;
   int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
@@ -1266,23 +1271,23 @@ cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_coop_kernel, mq, mk, mv, p, n_chain, flags);
+  return cudaLaunchKernelEx(&cfg, chunk_coop_kernel<DKP>, mq, mk, mv, p, n_chain, flags);
 }
 
-cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
+template <int DKP>
+cudaError_t launch_split_dk(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;  // mv: V in 64-column boxes for the prepare kernel's U~
   SplitParams p;
   if (!split_setup(a, workspace, mq, mk, mv, p)) return cudaErrorInvalidValue;
   static PerDeviceOnce attrs;
   const cudaError_t attr_err = attrs.run([] {
-    cudaError_t e = cudaFuncSetAttribute(chunk_prepare_kernel,
+    cudaError_t e = cudaFuncSetAttribute(chunk_prepare_kernel<DKP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_chain_kernel<SplitChain>,
+      e = cudaFuncSetAttribute(chunk_chain_kernel<SplitChain, DKP>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, SplitChain::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_chain_kernel<SplitChain64>,
+      e = cudaFuncSetAttribute(chunk_chain_kernel<SplitChain64, DKP>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, SplitChain64::kSmem);
     return e;
   });
@@ -1307,7 +1312,7 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   cfg.gridDim = dim3((unsigned)p.max_items);
   cfg.blockDim = dim3(kPrepThreads);
   cfg.dynamicSmemBytes = kPrepSmem;
-  e = cudaLaunchKernelEx(&cfg, chunk_prepare_kernel, mq, mk, mv, p);
+  e = cudaLaunchKernelEx(&cfg, chunk_prepare_kernel<DKP>, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
   // 64-row chain CTAs once the 32-row ones would need more than one wave
   int dev = 0, sms = 0;
@@ -1322,11 +1327,32 @@ cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStre
   if (wide) {
     cfg.blockDim = dim3(SplitChain64::kThreads);
     cfg.dynamicSmemBytes = SplitChain64::kSmem;
-    return cudaLaunchKernelEx(&cfg, chunk_chain_kernel<SplitChain64>, mq, mk, p);
+    return cudaLaunchKernelEx(&cfg, chunk_chain_kernel<SplitChain64, DKP>, mq, mk, p);
   }
   cfg.blockDim = dim3(SplitChain::kThreads);
   cfg.dynamicSmemBytes = SplitChain::kSmem;
-  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel<SplitChain>, mq, mk, p);
+  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel<SplitChain, DKP>, mq, mk, p);
+}
+
+}  // namespace
+
+cudaError_t launch_chunked_coop(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (!coop_supported(a.num_seqs, a.h_v, a.d_v, sms)) return cudaErrorNotSupported;
+  if (a.d_k == kDK) return launch_coop_dk<kDK>(a, workspace, stream, sms);
+  if (a.d_k == kDK / 2) return launch_coop_dk<kDK / 2>(a, workspace, stream, sms);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_chunked_split(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  if (a.d_k == kDK) return launch_split_dk<kDK>(a, workspace, stream);
+  if (a.d_k == kDK / 2) return launch_split_dk<kDK / 2>(a, workspace, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace gdn

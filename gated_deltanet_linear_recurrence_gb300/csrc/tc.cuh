@@ -94,6 +94,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Bring `bytes` (a multiple of 16, from a 16-byte aligned address) of global
+// memory into L2 without waiting.  A hint with no effect on memory ordering:
+// L2 is the point of coherence, so lines fetched early still show any later
+// write by another kernel.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
