@@ -86,7 +86,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype; /* dtype of q, k, v and o 
 #define GDN_OPT_QK_L2NORM 1u
 
 typedef enum {
-  GDN_ALGO_AUTO = 0,          /* per sequence: scan below the measured crossover length, else chunked */
+  GDN_ALGO_AUTO = 0,          /* by a table measured per shape: scan for short sequences, else
+                                 the fastest chunked form the call can run (see gdn_prefill) */
   GDN_ALGO_SCAN = 1,          /* token scan, state rows resident in registers (fp32 and bf16) */
   GDN_ALGO_CHUNKED = 2,       /* chunks of 64 tokens on tcgen05 tensor cores (bf16); the library
                                  picks the fused or the two-kernel form (see gdn_prefill) */
@@ -112,21 +113,28 @@ typedef enum {
  * non-decreasing, cu[num_seqs] = total_tokens; scale multiplies q (1 for the
  * plain reading o_t = S_t q_t).  algo selects the evaluation (see gdn_algo);
  * the chunked algorithms with GDN_F32 return GDN_ERR_UNSUPPORTED_DTYPE.
- * workspace: scratch, 16-byte aligned, or NULL.  The chunked evaluation runs
- * either as one fused kernel that needs no workspace, or as two kernels (the
- * per-chunk state-independent work spread over all SMs, then the sequential
- * state pass) that meet in the workspace.  GDN_ALGO_AUTO and GDN_ALGO_CHUNKED
- * take the two kernels when the sequences average at least 256 tokens (where
- * they measured faster on GB300) and workspace_bytes is at least
- * gdn_prefill_workspace_size(...), else the fused kernel;
- * GDN_ALGO_CHUNKED_SPLIT always takes them and returns GDN_ERR_NULL_POINTER or
- * GDN_ERR_WORKSPACE_TOO_SMALL without one.  The same work also runs as one
- * cooperative kernel whose prepare CTAs and state-pass CTAs overlap
- * (GDN_ALGO_CHUNKED_COOP; AUTO and CHUNKED take it when the sequences average at
- * least 4,096 tokens, its state passes fit and the workspace holds its ready
- * flags; its results equal the two kernels' bit for bit).  Results agree
- * within rounding; the
- * workspace is not used after the launches complete.
+ * workspace: scratch, 16-byte aligned, or NULL.  The chunked evaluation
+ * (bf16; d_k 128, or 64 with the two-kernel and cooperative forms, which pad
+ * each key head to 128 columns with zeros; d_v a multiple of 32) runs either
+ * as one fused kernel that needs no workspace (d_k 128 only), or as two
+ * kernels (the per-chunk state-independent work spread over all SMs, then the
+ * sequential state pass) that meet in the workspace, or as one cooperative
+ * kernel whose prepare CTAs and state-pass CTAs overlap (GDN_ALGO_CHUNKED_COOP;
+ * its results equal the two kernels' bit for bit).  GDN_ALGO_SCAN and the
+ * forced chunked forms run what they name; GDN_ALGO_CHUNKED_SPLIT and
+ * GDN_ALGO_CHUNKED_COOP return GDN_ERR_NULL_POINTER or
+ * GDN_ERR_WORKSPACE_TOO_SMALL without the workspace they need.
+ * GDN_ALGO_AUTO and GDN_ALGO_CHUNKED choose by a table measured on GB300 per
+ * (d_k, d_v, h_v, num_seqs) (the nearest measured shape): sequences shorter
+ * than its scan threshold take the token scan (the whole batch when the
+ * sequences average less; AUTO only); the others the fused kernel, or the two
+ * kernels from the table's average length when workspace_bytes is at least
+ * gdn_prefill_workspace_size(...) (always, when the fused kernel does not
+ * cover the call; with too little workspace AUTO then scans and CHUNKED
+ * returns GDN_ERR_WORKSPACE_TOO_SMALL), or the cooperative form from its
+ * average length when its state passes fit and the workspace holds its ready
+ * flags.  gdn_prefill_form reports the choice for given sizes.  Results agree
+ * within rounding; the workspace is not used after the launches complete.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g,
                        const float* beta, const float* state_in, float* state_out, void* o,
@@ -170,8 +178,8 @@ size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *
  * Same tensors as gdn_prefill for one sequence (no cu_seqlens: the sequence is
  * tokens 0 .. total_tokens-1); state_in may be NULL (zeros) or equal state_out.
- * Every piece runs the two-kernel chunked evaluation (bf16, d_k 128, d_v a
- * multiple of 32), else the token scan, so the result equals bit for bit
+ * Every piece runs the two-kernel chunked evaluation (bf16, d_k 128 or 64,
+ * d_v a multiple of 32), else the token scan, so the result equals bit for bit
  * gdn_prefill with GDN_ALGO_CHUNKED_SPLIT (resp. GDN_ALGO_SCAN) on the whole
  * sequence.  workspace: required, 16-byte aligned, at least
  * gdn_prefill_streamed_workspace_size(piece_tokens, ...) bytes, which does not
@@ -237,8 +245,8 @@ size_t gdn_prefill_host_workspace_size(int64_t piece_tokens, int32_t h_k, int32_
  * allocates nothing and calls no allocating routine.
  *
  * Arguments, layouts, ownership of the caller's buffers and asynchronous
- * errors are those of gdn_prefill; dtype must be GDN_BF16, d_k 128 and d_v a
- * multiple of 32 (else GDN_ERR_UNSUPPORTED_*).  Limit: returns
+ * errors are those of gdn_prefill; dtype must be GDN_BF16, d_k 128 or 64 and d_v
+ * a multiple of 32 (else GDN_ERR_UNSUPPORTED_*).  Limit: returns
  * GDN_ERR_WORKSPACE_TOO_SMALL, touching no device, when
  * gdn_prefill_workspace_size(..., GDN_ALGO_CHUNKED_SPLIT) for these arguments
  * exceeds GDN_NOALLOC_SCRATCH_BYTES (96 MiB: e.g. one 4,096-token sequence at
@@ -420,8 +428,10 @@ int32_t gdn_prefill_form(int32_t num_seqs, int64_t total_tokens, int32_t h_k, in
 /*
  * gdn_prefill_crossover_tokens — the sequence length at and above which
  * GDN_ALGO_AUTO uses the chunked evaluation for these head dimensions and
- * dtype (a table measured on GB300); shorter sequences use the token scan.
- * Returns INT32_MAX when the chunked evaluation does not support the case.
+ * dtype, for a single sequence (the table measured on GB300; a batch of N
+ * sequences may take another threshold, which gdn_prefill_form applies);
+ * shorter sequences use the token scan.  Returns INT32_MAX when the chunked
+ * evaluation does not support the case.
  */
 int32_t gdn_prefill_crossover_tokens(int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v,
                                      gdn_dtype dtype);
