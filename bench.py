@@ -649,6 +649,30 @@ def bench_decode(torch, gdn_decode_step, inputs, dev, stream, peaks, args, flush
                                     "frac_of_measured_hbm": nbytes / (qms / 1e3) / 1e9 /
                                     peaks["hbm_gbs"]}
 
+    # the same step with the output RMS normalisation fused in (gdn_decode_step_rmsnorm)
+    from gated_deltanet_linear_recurrence_gb300 import gdn_decode_step_rmsnorm
+    wn = torch.ones(w["d_v"], dtype=torch.float32, device=dev)
+
+    def nstep():
+        gdn_decode_step_rmsnorm(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"],
+                                norm_weight=wn, o=o, stream=stream)
+
+    for _ in range(args.warmup):
+        nstep()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        nstep()
+        b.record(stream)
+    torch.cuda.synchronize()
+    nms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    out["decode_b256_out_rmsnorm"] = {"us_per_step": nms * 1e3,
+                                      "gbs": nbytes / (nms / 1e3) / 1e9,
+                                      "frac_of_measured_hbm": nbytes / (nms / 1e3) / 1e9 /
+                                      peaks["hbm_gbs"]}
+
     # the same 256 sequences advanced by 4 tokens in one launch (gdn_decode_multi),
     # without and with the per-token state snapshots
     from gated_deltanet_linear_recurrence_gb300 import gdn_decode_multi

@@ -14,7 +14,8 @@ from ._lib import GdnError, STATUS_NAMES
 
 __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspace_size",
            "gdn_prefill_host", "gdn_prefill_host_workspace_size",
-           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_multi", "gdn_attn_decode",
+           "gdn_prefill_noalloc", "gdn_decode_step", "gdn_decode_step_rmsnorm",
+           "gdn_output_rmsnorm", "gdn_decode_multi", "gdn_attn_decode",
            "gdn_attn_decode_workspace_size", "gdn_attn_decode_block_keys",
            "gdn_prefill_workspace_size",
            "gdn_stream_status", "gdn_status_string", "gdn_prefill_crossover_tokens",
@@ -250,6 +251,50 @@ def gdn_decode_step(q, k, v, g, beta, state, o=None, scale=1.0, stream=None, qk_
                                 _ptr(o), B, h_k, h_v, d_k, d_v, dt, float(scale),
                                 _options(qk_l2norm), _stream(stream))
     _lib.check(st, "gdn_decode_step")
+    return o
+
+
+def gdn_decode_step_rmsnorm(q, k, v, g, beta, state, norm_weight=None, norm_eps=1e-6, o=None,
+                            scale=1.0, stream=None, qk_l2norm=False):
+    """gdn_decode_step with the output RMS-normalised in the same kernel
+    (gdn_decode_step_rmsnorm in include/gdn.h): o[b, h] = w * y / rms(y) over the
+    d_v values, norm_weight [d_v] fp32 or None (ones)."""
+    lib = _lib.load()
+    B, h_k, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    _require(k.shape == q.shape and v.shape[0] == B, "q/k/v shapes disagree")
+    _require(state.shape == (B, h_v, d_v, d_k) and state.dtype == torch.float32,
+             "state must be [B, h_v, d_v, d_k] fp32")
+    _require(g.dtype == torch.float32 and beta.dtype == torch.float32, "g/beta must be fp32")
+    if norm_weight is not None:
+        _require(norm_weight.shape == (d_v,) and norm_weight.dtype == torch.float32,
+                 "norm_weight must be [d_v] fp32")
+    for t in (q, k, v, g, beta, state, norm_weight):
+        _require(t is None or t.is_contiguous(), "tensors must be contiguous")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((B, h_v, d_v), dtype=q.dtype, device=q.device)
+    st = lib.gdn_decode_step_rmsnorm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                     _ptr(o), _ptr(norm_weight), float(norm_eps), B, h_k, h_v,
+                                     d_k, d_v, dt, float(scale), _options(qk_l2norm),
+                                     _stream(stream))
+    _lib.check(st, "gdn_decode_step_rmsnorm")
+    return o
+
+
+def gdn_output_rmsnorm(o, norm_weight=None, norm_eps=1e-6, stream=None):
+    """The output RMS normalisation in place over o [..., h_v, d_v] (gdn_output_rmsnorm
+    in include/gdn.h); returns o."""
+    lib = _lib.load()
+    _require(o.dim() >= 2 and o.is_contiguous(), "o must be contiguous [..., h_v, d_v]")
+    h_v, d_v = o.shape[-2], o.shape[-1]
+    rows = o.numel() // (h_v * d_v) if o.numel() else 0
+    if norm_weight is not None:
+        _require(norm_weight.shape == (d_v,) and norm_weight.dtype == torch.float32 and
+                 norm_weight.is_contiguous(), "norm_weight must be [d_v] fp32")
+    st = lib.gdn_output_rmsnorm(_ptr(o), _ptr(norm_weight), rows, h_v, d_v, _dtype_code(o),
+                                float(norm_eps), _stream(stream))
+    _lib.check(st, "gdn_output_rmsnorm")
     return o
 
 

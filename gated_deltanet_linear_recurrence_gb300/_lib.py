@@ -49,6 +49,10 @@ SIGNATURES = {
                                            _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                        _i32, ctypes.c_int, _f32, _vp]),
+    "gdn_decode_step_rmsnorm": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32,
+                                               _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32,
+                                               ctypes.c_uint32, _vp]),
+    "gdn_output_rmsnorm": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, ctypes.c_int, _f32, _vp]),
     "gdn_decode_multi": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                         _i32, _i32, _i32, ctypes.c_int, _f32, ctypes.c_uint32,
                                         _vp]),

@@ -26,22 +26,19 @@ namespace {
 
 constexpr int kDecodeWarps = 4;
 
+// The step for the warp's rows row0 ..: loads, update and in-place store of the
+// state rows; returns this lane's output value, and whether the lane holds one
+// (mine) for row row_mine.
 template <int DK, int R, bool kPrefetch, typename T>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-    decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                       const float* __restrict__ g, const float* __restrict__ beta,
-                       float* __restrict__ state, T* __restrict__ o, int32_t h_k, int32_t h_v,
-                       int32_t d_v, int32_t blocks_per_head, float scale, int qk_norm) {
+__device__ __forceinline__ float step_rows(const T* __restrict__ q, const T* __restrict__ k,
+                                           const T* __restrict__ v, const float* __restrict__ g,
+                                           const float* __restrict__ beta,
+                                           float* __restrict__ state, int32_t h_k, int32_t h_v,
+                                           int32_t d_v, float scale, int qk_norm, int b, int h,
+                                           int row0, int lane, int& row_mine, bool& mine) {
   constexpr int L = DK / 4;  // one float4 per lane per row
   using LY = RowLayout<DK, L, R>;
   constexpr int M = LY::M;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int b = blockIdx.x / blocks_per_head;
-  const int rb = blockIdx.x - b * blocks_per_head;
-  const int h = blockIdx.y;
-  const int row0 = (rb * kDecodeWarps + warp) * LY::kRowsPerWarp;
-  if (row0 >= d_v) return;  // whole warp idle (d_v is a multiple of 16)
   const int grp = lane / L;
   const int lam = lane % L;
   const int hk = h / (h_v / h_k);
@@ -90,7 +87,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
   const int idx = lam / LY::Q;  // reduced value index this lane will hold
   const int r_mine = idx >> 1;
-  const int row_mine = row0 + r_mine * LY::G + grp;
+  row_mine = row0 + r_mine * LY::G + grp;
   const float v_mine = load1(v + bh * d_v + row_mine);
   const float alpha = expf(__ldg(g + bh));
   const float bt = __ldg(beta + bh);
@@ -101,43 +98,115 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   kq = group_sum<L>(kq);
 
   const float out = row_token_update<DK, L, R>(s, k4, q4, kq, alpha, bt, v_mine, lane);
-  if ((idx & 1) && (lam % LY::Q) == 0) store1(o + bh * d_v + row_mine, out);
+  mine = (idx & 1) && (lam % LY::Q) == 0;
 
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int m = 0; m < M; ++m)
       __stcs(reinterpret_cast<float4*>(srow + (int64_t)r * LY::G * DK + 4 * L * m), s[r][m]);
+  return out;
 }
 
-template <int DK, int R, bool kPrefetch, typename T>
+// Output RMS normalisation fused into the step (kNorm): the CTAs of one
+// (sequence, value head) form a thread-block cluster; each sums the squares of
+// its rows' outputs, the partial sums are exchanged through distributed shared
+// memory, and every CTA scales its own outputs before storing them.
+struct OutNorm {
+  const float* weight;  // [d_v] or NULL (ones)
+  float eps;
+};
+
+template <int DK, int R, bool kPrefetch, bool kNorm, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                       const float* __restrict__ g, const float* __restrict__ beta,
+                       float* __restrict__ state, T* __restrict__ o, int32_t h_k, int32_t h_v,
+                       int32_t d_v, int32_t blocks_per_head, float scale, int qk_norm,
+                       OutNorm nrm) {
+  constexpr int L = DK / 4;  // one float4 per lane per row
+  using LY = RowLayout<DK, L, R>;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int b = blockIdx.x / blocks_per_head;
+  const int rb = blockIdx.x - b * blocks_per_head;
+  const int h = blockIdx.y;
+  const int row0 = (rb * kDecodeWarps + warp) * LY::kRowsPerWarp;
+  if constexpr (kNorm) {
+    // every warp takes part in the cluster's reduction, idle ones with nothing
+    __shared__ float part[kDecodeWarps + 1];
+    float sq = 0.f, out = 0.f;
+    int row_mine = 0;
+    bool mine = false;
+    if (row0 < d_v)
+      out = step_rows<DK, R, kPrefetch>(q, k, v, g, beta, state, h_k, h_v, d_v, scale, qk_norm,
+                                        b, h, row0, lane, row_mine, mine);
+    if (mine) sq = out * out;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(kFullMask, sq, off);
+    if (lane == 0) part[warp] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) t += part[w];
+      part[kDecodeWarps] = t;
+    }
+    tc::cluster_sync();  // every CTA's partial sum is written
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+      for (int r = 0; r < blocks_per_head; ++r) t += tc::ld_cluster_f32(&part[kDecodeWarps], r);
+      part[0] = rsqrtf(t / (float)d_v + nrm.eps);  // own slot 0 is read by no other CTA
+    }
+    tc::cluster_sync();  // the partial sums have been read: no CTA leaves before that
+    if (mine) {
+      const float wgt = nrm.weight ? __ldg(nrm.weight + row_mine) : 1.f;
+      store1(o + ((int64_t)b * h_v + h) * d_v + row_mine, out * part[0] * wgt);
+    }
+  } else {
+    if (row0 >= d_v) return;  // whole warp idle (d_v is a multiple of 16)
+    int row_mine;
+    bool mine;
+    const float out = step_rows<DK, R, kPrefetch>(q, k, v, g, beta, state, h_k, h_v, d_v, scale,
+                                                  qk_norm, b, h, row0, lane, row_mine, mine);
+    if (mine) store1(o + ((int64_t)b * h_v + h) * d_v + row_mine, out);
+  }
+}
+
+template <int DK, int R, bool kPrefetch, bool kNorm, typename T>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int L = DK / 4;
   constexpr int rows_per_block = kDecodeWarps * RowLayout<DK, L, R>::kRowsPerWarp;
   const int blocks_per_head = (a.d_v + rows_per_block - 1) / rows_per_block;
   const int64_t gx = (int64_t)a.batch * blocks_per_head;
   if (gx > 0x7fffffffLL || a.h_v > 65535) return cudaErrorInvalidConfiguration;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // the CTAs of one (sequence, head)
+  attr[1].val.clusterDim.x = (unsigned)blocks_per_head;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  if (kNorm && blocks_per_head > 8) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx, (unsigned)a.h_v);
   cfg.blockDim = dim3(kDecodeWarps * 32);
   cfg.stream = stream;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_step_kernel<DK, R, kPrefetch, T>,
-                            static_cast<const T*>(a.q),
-                            static_cast<const T*>(a.k), static_cast<const T*>(a.v), a.g, a.beta,
-                            a.state, static_cast<T*>(a.o), a.h_k, a.h_v, a.d_v, blocks_per_head,
-                            a.scale, a.qk_norm);
+  cfg.attrs = attr;
+  cfg.numAttrs = kNorm ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<DK, R, kPrefetch, kNorm, T>,
+                            static_cast<const T*>(a.q), static_cast<const T*>(a.k),
+                            static_cast<const T*>(a.v), a.g, a.beta, a.state, static_cast<T*>(a.o),
+                            a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale, a.qk_norm,
+                            OutNorm{a.norm_weight, a.norm_eps});
 }
 
 // Rows per lane group: R = L/2 gives 16 rows per warp (most bytes in flight
 // per warp); with few rows in total a smaller R spreads the work over more SMs,
 // and the state is prefetched into L2 ahead of the dependency wait (measured
 // on GB300, batch 1 through 30 layers in one CUDA graph: 78.3 -> 70.1 us per
-// step; 8 rows per warp instead of 4 measured 86.5 us).
+// step; 8 rows per warp instead of 4 measured 86.5 us).  With the output
+// normalisation a head's CTAs (at most 8) form one cluster.
 template <int DK, typename T>
 cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int L = DK / 4;
@@ -145,9 +214,12 @@ cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int R_SMALL = (L / 8) > 0 ? (L / 8) : 1;
   const int64_t rows = (int64_t)a.batch * a.h_v * a.d_v;
   // 16 rows per warp still gives >= 4 warps on every one of 152 SMs
-  if (rows >= (int64_t)16 * 4 * 152 * kDecodeWarps)
-    return launch_t<DK, R_BIG, false, T>(a, stream);
-  return launch_t<DK, R_SMALL, true, T>(a, stream);
+  const bool big = rows >= (int64_t)16 * 4 * 152 * kDecodeWarps;
+  if (a.out_norm)
+    return big ? launch_t<DK, R_BIG, false, true, T>(a, stream)
+               : launch_t<DK, R_SMALL, true, true, T>(a, stream);
+  return big ? launch_t<DK, R_BIG, false, false, T>(a, stream)
+             : launch_t<DK, R_SMALL, true, false, T>(a, stream);
 }
 
 template <typename T>

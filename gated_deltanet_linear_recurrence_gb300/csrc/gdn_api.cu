@@ -436,6 +436,51 @@ gdn_status gdn_decode_step_ex(const void* q, const void* k, const void* v, const
   return GDN_OK;
 }
 
+gdn_status gdn_decode_step_rmsnorm(const void* q, const void* k, const void* v, const float* g,
+                                   const float* beta, float* state, void* o,
+                                   const float* norm_weight, float norm_eps, int32_t batch,
+                                   int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v,
+                                   gdn_dtype dtype, float scale, uint32_t options,
+                                   gdn_stream_t stream) {
+  if (batch < 0) return GDN_ERR_INVALID_ARG;
+  if (options & ~static_cast<uint32_t>(GDN_OPT_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
+  if (!(norm_eps >= 0.f) || norm_eps > 3.0e38f) return GDN_ERR_INVALID_ARG;  // NaN too
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  gdn_status st = check_heads(h_k, h_v, d_k, d_v);
+  if (st != GDN_OK) return st;
+  if (batch == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !state || !o) return GDN_ERR_NULL_POINTER;
+  const void* ptrs[] = {q, k, v, g, beta, state, o, norm_weight};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  gdn::DecodeArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.o = o;
+  a.batch = batch; a.h_k = h_k; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v;
+  a.dtype = dtype; a.scale = scale;
+  a.qk_norm = (options & GDN_OPT_QK_L2NORM) ? 1 : 0;
+  a.out_norm = 1;
+  a.norm_weight = norm_weight;
+  a.norm_eps = norm_eps;
+  if (gdn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+gdn_status gdn_output_rmsnorm(void* o, const float* norm_weight, int64_t rows, int32_t h_v,
+                              int32_t d_v, gdn_dtype dtype, float norm_eps, gdn_stream_t stream) {
+  if (rows < 0 || h_v <= 0 || d_v <= 0) return GDN_ERR_INVALID_ARG;
+  if (!(norm_eps >= 0.f) || norm_eps > 3.0e38f) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED_DTYPE;
+  if (!head_dim_ok(d_v) || h_v > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return GDN_OK;
+  if (!o) return GDN_ERR_NULL_POINTER;
+  if (!aligned16(o) || (norm_weight && !aligned16(norm_weight))) return GDN_ERR_MISALIGNED;
+  if (gdn::launch_output_rmsnorm(o, norm_weight, rows * h_v, d_v, dtype, norm_eps,
+                                 reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
 gdn_status gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, float* state, void* o, float* snapshots,
                             int32_t batch, int32_t n_tokens, int32_t h_k, int32_t h_v,

@@ -24,6 +24,11 @@ struct DecodeArgs {
   int dtype;
   float scale;
   int qk_norm;  // divide q and k by their L2 norm (+1e-6 under the root) first
+  // Output RMS normalisation in the same kernel (out_norm != 0): o[b,h,:] scaled
+  // by w / sqrt(mean of its squares + norm_eps); norm_weight [d_v] or NULL (ones).
+  int out_norm;
+  const float* norm_weight;
+  float norm_eps;
 };
 
 // Several tokens per sequence: q, k [B][n][h_k][d_k], v, o [B][n][h_v][d_v],
@@ -100,6 +105,9 @@ AttnPlan attn_plan(int32_t batch, int32_t h_kv, int32_t capacity, int layout, in
 size_t attn_partial_bytes(int32_t batch, int32_t h_q, const AttnPlan& plan);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// The output RMS normalisation in place over n_vec vectors of d_v values (output_norm.cu).
+cudaError_t launch_output_rmsnorm(void* o, const float* weight, int64_t n_vec, int32_t d_v,
+                                  int dtype, float eps, cudaStream_t stream);
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const PrefillArgs& a, cudaStream_t stream);

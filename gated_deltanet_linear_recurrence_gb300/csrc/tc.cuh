@@ -286,6 +286,28 @@ __device__ __forceinline__ float fast_exp(float x) {
   return y;
 }
 
+// ------------------------------------------------------------------ clusters
+// All threads of every CTA of the cluster: arrive (releasing this thread's
+// earlier shared-memory writes to the cluster), then wait for everyone.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Load a float from the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------ dependent launch
 // Programmatic dependent launch: the next kernel in the stream may start its
 // set-up now; and this kernel's reads of the previous kernel's results wait

@@ -293,6 +293,41 @@ gdn_status gdn_decode_step_ex(const void* q, const void* k, const void* v, const
                               float scale, uint32_t options, gdn_stream_t stream);
 
 /*
+ * gdn_decode_step_rmsnorm — gdn_decode_step_ex with the layer's output
+ * normalised inside the same kernel.  Page "Optimizing on-device inference for
+ * Apple Silicon", section "Reduce intermediate and state traffic": the decode
+ * path fuses the recurrent update with its normalization; the page does not
+ * give the normalisation's form, and this entry point takes the plainest one
+ * for an output: a root-mean-square normalisation of each (sequence, value
+ * head)'s d_v outputs with a per-channel weight shared by the heads,
+ *
+ *     o[b,h,i] = w_i * y_i / sqrt( (1 / d_v) sum_j y_j^2 + norm_eps )
+ *
+ * where y is the step's output in fp32 (before rounding to `dtype`).
+ * norm_weight: [d_v] fp32, 16-byte aligned, or NULL for w = 1; norm_eps >= 0
+ * (else GDN_ERR_INVALID_ARG).  The state update is exactly gdn_decode_step_ex's
+ * (bit for bit).  The CTAs that share a (sequence, head) form one thread-block
+ * cluster and exchange their partial sums of squares through distributed
+ * shared memory, so o is written once, already normalised.
+ */
+gdn_status gdn_decode_step_rmsnorm(const void* q, const void* k, const void* v, const float* g,
+                                   const float* beta, float* state, void* o,
+                                   const float* norm_weight, float norm_eps, int32_t batch,
+                                   int32_t h_k, int32_t h_v, int32_t d_k, int32_t d_v,
+                                   gdn_dtype dtype, float scale, uint32_t options,
+                                   gdn_stream_t stream);
+
+/*
+ * gdn_output_rmsnorm — the same normalisation as a pass of its own, in place,
+ * over o [rows][h_v][d_v] in `dtype` (for example a gdn_prefill output; the
+ * values are those stored in o, already rounded to `dtype`).  norm_weight and
+ * norm_eps as for gdn_decode_step_rmsnorm; d_v one of 16, 32, 64, 128.
+ * Reads and writes o once.
+ */
+gdn_status gdn_output_rmsnorm(void* o, const float* norm_weight, int64_t rows, int32_t h_v,
+                              int32_t d_v, gdn_dtype dtype, float norm_eps, gdn_stream_t stream);
+
+/*
  * gdn_decode_multi — n_tokens (1 .. 1024) consecutive tokens for each of
  * `batch` sequences in one launch: the state is read once, carried through the
  * tokens and written once.  Page "Optimizing on-device inference for Apple

@@ -340,3 +340,35 @@ def test_prefill_form_python_names():
         f(4096, algo="chunked_coop")          # no workspace
     with pytest.raises(GdnError):
         f(4096, algo="chunked_fused", qk_l2norm=True)
+
+
+def test_output_norm_host_errors(lib):
+    """The output RMS normalisation entry points refuse bad arguments before
+    launching anything (no device is touched)."""
+    def dec(b=2, h_k=1, h_v=2, d_k=16, d_v=16, dtype=1, eps=1e-6, w=None, opts=0, **ptr):
+        p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE)
+        p.update(ptr)
+        return lib.gdn_decode_step_rmsnorm(p["q"], p["k"], p["v"], p["g"], p["beta"], p["state"],
+                                           p["o"], w, eps, b, h_k, h_v, d_k, d_v, dtype, 1.0,
+                                           opts, None)
+    assert dec(b=0) == 0                      # nothing to do
+    assert dec(b=-1) == 2
+    assert dec(eps=-1.0) == 2                 # eps must be >= 0
+    assert dec(eps=float("nan")) == 2
+    assert dec(opts=4) == 2
+    assert dec(dtype=7) == 4
+    assert dec(d_v=48) == 3
+    assert dec(o=None) == 1
+    assert dec(w=FAKE + 4) == 5               # misaligned weight
+
+    def norm(rows=4, h_v=2, d_v=64, dtype=1, eps=1e-6, o=FAKE, w=None):
+        return lib.gdn_output_rmsnorm(o, w, rows, h_v, d_v, dtype, eps, None)
+    assert norm(rows=0) == 0
+    assert norm(rows=-1) == 2
+    assert norm(h_v=0) == 2
+    assert norm(eps=-0.5) == 2
+    assert norm(d_v=24) == 3
+    assert norm(dtype=3) == 4
+    assert norm(o=None) == 1
+    assert norm(o=FAKE + 2) == 5
+    assert norm(w=FAKE + 8) == 5

@@ -11,7 +11,8 @@ import pytest
 import torch
 
 from gated_deltanet_linear_recurrence_gb300 import (gdn_attn_decode, gdn_decode_multi,
-                                                    gdn_decode_step, gdn_prefill,
+                                                    gdn_decode_step, gdn_decode_step_rmsnorm,
+                                                    gdn_output_rmsnorm, gdn_prefill,
                                                     gdn_stream_status, inputs)
 
 pytestmark = pytest.mark.gpu
@@ -71,6 +72,22 @@ def test_decode_step_writes_stay_inside_state_and_o():
     gdn_decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], st.t, o=o.t)
     assert gdn_stream_status() == "GDN_OK"
     assert st.intact() and o.intact()
+
+
+def test_normalised_decode_and_norm_pass_write_inside_their_buffers():
+    B, h_k, h_v, d_k, d_v = 3, 2, 4, 128, 64
+    x = dev(inputs.make_decode(B, h_k, h_v, d_k, d_v, "bf16", seed=215))
+    st = Canaried((B, h_v, d_v, d_k), torch.float32, seed=8)
+    st.t.copy_(x["state"])
+    o = Canaried((B, h_v, d_v), torch.bfloat16, seed=9)
+    w = torch.ones(d_v, dtype=torch.float32, device="cuda")
+    gdn_decode_step_rmsnorm(x["q"], x["k"], x["v"], x["g"], x["beta"], st.t, norm_weight=w,
+                            o=o.t)
+    assert gdn_stream_status() == "GDN_OK"
+    assert st.intact() and o.intact()
+    gdn_output_rmsnorm(o.t, norm_weight=w)
+    assert gdn_stream_status() == "GDN_OK"
+    assert o.intact()
 
 
 def test_decode_multi_writes_stay_inside_state_and_o():
