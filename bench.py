@@ -40,12 +40,21 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "66ba0d5189080d55",
-                    "bytes": (68_254_720 + 31_455_488) + (118_787_840 + 11_955_968),
+                    "sha256_16": "40b9cf8e161f5350",
+                    "bytes": (68_258_816 + 31_124_736) + (118_789_888 + 12_016_384),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                   "sha256_16": "66ba0d5189080d55", "bytes": 68_641_792 + 67_524_352,
+                   "sha256_16": "40b9cf8e161f5350", "bytes": 68_702_720 + 66_749_696,
                    "profile": "profiles/chunk_coop_t4096.md"},
+    "chunk_coop@prefill_t131072": {
+        "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
+        "sha256_16": "40b9cf8e161f5350", "bytes": 5_413_437_952 + 3_772_615_168,
+        "profile": "profiles/chunk_coop_t131072.md"},
+    "chunk_split@prefill_varlen10": {
+        "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
+        "sha256_16": "40b9cf8e161f5350",
+        "bytes": 12_800 + (4_363_545_088 + 5_380_021_248) + (7_594_119_168 + 2_140_511_488),
+        "profile": "profiles/chunk_split_varlen10.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
                       "profile": "profiles/chunk_prefill_t4096.md"},
@@ -53,7 +62,7 @@ NCU_TRAFFIC = {
                     "sha256_16": "5f6befb361bfe092", "bytes": 268_506_368 + 2_978_048,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
-                    "sha256_16": "620ed98dc0429f3d", "bytes": 541_154_304 + 479_891_712,
+                    "sha256_16": "6bc3ccc0013040f8", "bytes": 541_250_560 + 480_322_304,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
@@ -280,6 +289,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="with --kernel-only prefill: the prompt's length instead of 4096")
     ap.add_argument("--no-long-prefill", action="store_true",
                     help="skip the 128K-token and ten-prompt varlen prefill timings")
     ap.add_argument("--sweep", action="store_true",
@@ -1036,7 +1047,9 @@ def run_kernel_only(args):
             gdn_decode_step(y["q"], y["k"], y["v"], y["g"], y["beta"], y["state"], o=o)
     else:
         name = WORKLOAD if args.kernel_only == "prefill" else args.kernel_only
-        w = inputs.WORKLOADS[name]
+        w = dict(inputs.WORKLOADS[name])
+        if args.kernel_only == "prefill" and args.tokens > 0:
+            w["lengths"] = [args.tokens]  # the same heads and distributions, another length
         d = inputs.make_prefill(w["lengths"], w["h_k"], w["h_v"], w["d_k"], w["d_v"],
                                 w["dtype"], seed=w["seed"], state_std=w["state_std"])
         x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
