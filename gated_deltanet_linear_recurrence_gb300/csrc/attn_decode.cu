@@ -180,9 +180,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
     const uint64_t dK0 = tc::smem_desc(sbase, 16, 1024, tc::kLayoutSw128);
     const uint64_t dV0 = tc::smem_desc(sbase + AS_V, 8192, 1024, tc::kLayoutSw128);
     const uint64_t dP0 = tc::smem_desc(sbase + AS_P, 16, 1024, tc::kLayoutSw128);
+    const bool leader = tc::elect_one();  // issues every product and commit of this warp
     auto issue_s = [&](int i) {  // S^T = K Q^T into S buffer i & 1
       const uint64_t so = (uint64_t)(((i % kAStages) * AS_STAGE) >> 4);
-      if (tc::elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
           tc::mma_bf16(tmem + TA_S + 8 * (i & 1),
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
       }
       if (!(ok = warp_wait(&p_ready[i & 1], (i >> 1) & 1))) break;
       const uint64_t so = (uint64_t)(((i % kAStages) * AS_STAGE) >> 4);
-      if (tc::elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb)    // dims 64 kb .. 64 kb + 63
 #pragma unroll
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
       __syncwarp();
     }
     // every MMA this warp issued has finished before TMEM is released
-    if (tc::elect_one()) tc::mma_commit(drained);
+    if (leader) tc::mma_commit(drained);
     __syncwarp();
     if (!warp_wait(drained, 0)) ok = false;
   } else {

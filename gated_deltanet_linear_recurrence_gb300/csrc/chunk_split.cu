@@ -707,7 +707,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   if (tid == 0) {
     for (int i = 0; i < NSTG; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&empty[i], 2);  // after D and after the state update
       tc::mbar_init(&tfull[i], 1);
       tc::mbar_init(&tempty[i], 2 * kEpiThreads / 4);
     }
@@ -779,32 +779,34 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
     const uint64_t dP0 =
         tc::smem_desc(sbase + CF::CC_TAIL - 8192, 16, 1024, tc::kLayoutSw128);
+    const bool leader = tc::elect_one();  // issues every product and commit of this warp
     for (int c = 0; c < nchunks && ok; ++c) {
       const int st = c % NSTG;
       const uint64_t so = (uint64_t)((st * CF::kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
       const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
       const uint32_t td = tmem + CF::TC_D0 + DVS * (c % 3), to2 = tmem + CF::TC_O0 + DVS * (c % 3);
       if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
-      if (tc::elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // D = [U~; 0] + [-W; Q] S_s^T (preloaded buffer)
           tc::mma_bf16(td, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
                        dSS + ((kk * 1024) >> 4), CF::IDC_WQ, 1);
         tc::mma_commit(bar_d);
+        tc::mma_commit(&empty[st]);  // D has read -W and Q of the stage
       }
       __syncwarp();
       if (!(ok = warp_wait(bar_u, c & 1))) break;
-      if (tc::elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
           tc::mma_bf16(tmem + CF::TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4),
                        CF::IDC_SU, 1);
         tc::mma_commit(bar_s);
-        tc::mma_commit(&empty[st]);  // -W, Q, K and U~ of the stage consumed
+        tc::mma_commit(&empty[st]);  // the update has read K of the stage
       }
       __syncwarp();
       if (!(ok = warp_wait(&tfull[st], (c / NSTG) & 1))) break;
-      if (tc::elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
           tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), CF::IDC_PU, kk > 0);
@@ -941,6 +943,8 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
       if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
         ok = tc::mbar_wait(bar_d, c & 1) && ok;
+        if (c > 0)  // P U of the previous chunk has read the U buffers about to be rewritten
+          ok = tc::mbar_wait(&bar_o[(c - 1) % 3], ((c - 1) / 3) & 1) && ok;
         tc::fence_after_sync();
         const float dec_r = gates[64 + rl];
 #pragma unroll
@@ -963,6 +967,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       } else {
         if (c > 0) gam_prev = take_gates(c - 1);
         if (c + 1 < nchunks) preload(c + 1);  // the buffer's rows were read by output c - 2
+        ok = tc::mbar_wait(bar_d, c & 1) && ok;  // D has read the staged state rewritten below
       }
       ok = tc::mbar_wait(bar_s, c & 1) && ok;
       tc::fence_after_sync();
@@ -991,304 +996,6 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
   if (warp == 0) tc::tmem_dealloc(tmem, CF::kTmemCols);
 }
 
-// The state pass for 64 rows of a head (ChainCfg<64, NSTG, 8>: the same shared
-// memory layout and threads as chain_run's 64-row form), with the U and output
-// products issued as M = 64 MMAs: an M = 64 accumulator keeps its rows on
-// lanes 0-15 of every TMEM lane quarter, so the U epilogue (on the chunk-to-
-// chunk critical path) runs on one warp per SM sub-partition, each thread
-// converting one row's 32 values of one block, instead of on two warps per
-// sub-partition of the two lane quarters an M = 128 product's top half uses.
-// Per chunk c:
-//   D_U  = U~ + (-W) S^T       M=64  N=64 K=128 (onto the preloaded U~; TC_DU)
-//   D_O  = Q S^T               M=64  N=64 K=128 (TC_DO, triple-buffered)
-//   S^T += K^T (decayed U)     M=128 N=64 K=64  (onto Gamma_n S^T; TC_S)
-//   O2   = P U                 M=64  N=64 K=64  (TC_O2, triple-buffered)
-//   O    = Gamma D_O + O2
-// Warps 0-3 (one per lane quarter) form U and preload the next U~; warps 4-7
-// take the gates and write the output; all eight stage the state (warp w:
-// lane quarter w % 4, value block w / 4).  The arithmetic of every output and
-// state element is that of chain_run: results are bitwise equal.
-template <int NSTG, int DKP>
-__device__ __forceinline__ void chain_run64(const SplitParams& p, const CUtensorMap* tm_q,
-                                            const CUtensorMap* tm_k, uint8_t* smem, int n, int h,
-                                            int s, int tid, const int* item_flags) {
-  using CF = ChainCfg<64, NSTG, 8>;
-  constexpr int DVS = 64;
-  constexpr int kEpiThreads = 256;
-  constexpr uint32_t TC_DU = 0, TC_DO = 64, TC_O2 = 256, TC_S = 448;
-  constexpr uint32_t ID64 = tc::idesc_bf16_f32(64, 64, false, true);  // (-W | Q | P) x (S^T | U)
-  const int warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3;                  // TMEM lane quarter
-  const int b0 = warp >> 2;                 // value block of the state epilogue
-  const int jrow = 32 * qd + lane;          // state epilogue: row of S^T (key dim)
-  const int r64 = 16 * qd + (lane & 15);    // M = 64 epilogues: accumulator row (token)
-  const int blk = lane >> 4;                // ... and its 32-value block
-  const int hk = h / (p.h_v / p.h_k);
-  int64_t t_beg, t_end;
-  if (!seq_range(p, n, t_beg, t_end)) {  // reported by the plan kernel, or here for one sequence
-    if (p.single && tid == 0) raise_error(p.err, kErrBadCuSeqlens);
-    return;
-  }
-  const int64_t L = t_end - t_beg;
-  if (L < p.min_len) return;  // the token scan owns this sequence
-  const int nchunks = (int)((L + kC - 1) / kC);
-  const int64_t srow0 = ((int64_t)n * p.h_v + h) * p.d_v + s * DVS;
-
-  // mbarriers as in chain_run: full/tfull (copies landed), empty (the stage's
-  // products done), tempty (the output warps took the chunk's gates); bar_d
-  // (D_U done), bar_s (D_O and the state update done), bar_o (P U done, one per
-  // chunk modulo 3), bar_u (U staged), bar_ss (state staged).
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CF::CC_MISC);
-  uint64_t* empty = full + NSTG;
-  uint64_t* tfull = empty + NSTG;
-  uint64_t* tempty = tfull + NSTG;
-  uint64_t* bar_d = tempty + NSTG;
-  uint64_t* bar_s = bar_d + 1;
-  uint64_t* bar_u = bar_s + 1;
-  uint64_t* bar_ss = bar_u + 1;
-  uint64_t* bar_o = bar_ss + 1;  // one per chunk modulo 3
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 3);
-  if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 512);
-    tc::tmem_relinquish();
-  }
-  if (tid == 0) {
-    for (int i = 0; i < NSTG; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
-      tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 128);  // warps 4-7
-    }
-    tc::mbar_init(bar_d, 1);
-    tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_u, 128);  // warps 0-3
-    tc::mbar_init(bar_ss, kEpiThreads);
-    for (int i = 0; i < 3; ++i) tc::mbar_init(&bar_o[i], 1);
-    tc::fence_mbar_init();
-  }
-  tc::fence_before_sync();
-  tc::named_sync(kBarChainCta, CF::kThreads);
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t sbase = tc::smem_u32(smem);
-  const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-  bool ok = true;
-  wait_prerequisites();  // the packages and chunk table (set-up above overlapped the prepare)
-  const int64_t first_item = p.single ? h : (int64_t)p.chunk_base[n] * p.h_v + h;
-
-  if (warp == CF::kProducerWarp) {
-    if (lane == 0) {
-      tc::prefetch_tmap(tm_q);
-      tc::prefetch_tmap(tm_k);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c % NSTG;
-        const int64_t item = first_item + (int64_t)c * p.h_v;
-        const uint8_t* pkg = p.packages + item * kPkgBytes;
-        if (c >= NSTG) ok = tc::mbar_wait(&empty[st], ((c / NSTG) - 1) & 1);
-        if (ok && item_flags) ok = wait_item_flag(item_flags + item);
-        if (!ok) break;
-        uint8_t* dst = smem + st * CF::kMain;
-        const int32_t y = static_cast<int32_t>(t_beg + (int64_t)c * kC);
-        uint64_t* fb = &full[st];
-        tc::mbar_arrive_expect_tx(fb, CF::kMainTx);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          kq_load<DKP>(dst + kb * kHalf + SC_Q, tm_q, hk, kb, y, fb);
-          kq_load<DKP>(dst + kb * kHalf + SC_K, tm_k, hk, kb, y, fb);
-          bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
-        }
-        bulk_g2s(dst + SC_U, pkg + kPkgU + s * 2 * kPkgUSlice, 2 * kPkgUSlice, fb);
-        if (c >= NSTG) ok = tc::mbar_wait(&tempty[st], ((c / NSTG) - 1) & 1);
-        if (!ok) break;
-        tc::mbar_arrive_expect_tx(&tfull[st], kTailTx);
-        bulk_g2s(smem + CF::CC_TAIL + st * kTail, pkg + kPkgP, 8192, &tfull[st]);
-        bulk_g2s(smem + CF::CC_GATE + st * kGateBytes, pkg + kPkgGates, kGateBytes, &tfull[st]);
-      }
-    }
-  } else if (warp == CF::kMmaWarp) {
-    // One warp issues every product (converged loop, one elected lane issues).
-    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-      const bool w = tc::mbar_wait(bar, parity);
-      tc::fence_after_sync();
-      return __all_sync(kFullMask, w) != 0;
-    };
-    const uint64_t dSS = tc::smem_desc(sbase + CF::CC_SS, 8192, 512, tc::kLayoutSw64);
-    const uint64_t dUK = tc::smem_desc(sbase + CF::CC_UK, 4096, 512, tc::kLayoutSw64);
-    const uint64_t dUB = tc::smem_desc(sbase + CF::CC_UB, 4096, 512, tc::kLayoutSw64);
-    const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
-    const uint64_t dQ0 = tc::smem_desc(sbase + SC_Q, 16, 1024, tc::kLayoutSw128);
-    const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
-    const uint64_t dP0 = tc::smem_desc(sbase + CF::CC_TAIL, 16, 1024, tc::kLayoutSw128);
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % NSTG;
-      const uint64_t so = (uint64_t)((st * CF::kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
-      const uint64_t dW = dW0 + so, dQ = dQ0 + so, dK = dK0 + so, dP = dP0 + to;
-      const uint32_t tdo = tmem + TC_DO + DVS * (c % 3), to2 = tmem + TC_O2 + DVS * (c % 3);
-      if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // D_U = U~ + (-W) S^T (preloaded buffer)
-          tc::mma_bf16(tmem + TC_DU, dW + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
-                       dSS + ((kk * 1024) >> 4), ID64, 1);
-        tc::mma_commit(bar_d);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // D_O = Q S^T
-          tc::mma_bf16(tdo, dQ + (((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
-                       dSS + ((kk * 1024) >> 4), ID64, kk > 0);
-      }
-      __syncwarp();
-      if (!(ok = warp_wait(bar_u, c & 1))) break;
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
-          tc::mma_bf16(tmem + TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4),
-                       CF::IDC_SU, 1);
-        tc::mma_commit(bar_s);       // also covers D_O, which read the staged state
-        tc::mma_commit(&empty[st]);  // -W, Q, K and U~ of the stage consumed
-      }
-      __syncwarp();
-      if (!(ok = warp_wait(&tfull[st], (c / NSTG) & 1))) break;
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // O2 = P U
-          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), ID64, kk > 0);
-        tc::mma_commit(&bar_o[c % 3]);
-      }
-      __syncwarp();
-    }
-  } else if (warp < 8) {
-    auto take_gates = [&](int cp) {
-      const int stp = cp % NSTG;
-      // P U of chunk cp + 3 is issued only after these warps stage chunk cp + 3's
-      // state, later than this wait, so the phase parity is unambiguous
-      ok = tc::mbar_wait(&bar_o[cp % 3], (cp / 3) & 1) && ok;
-      tc::fence_after_sync();
-      const float gr =
-          reinterpret_cast<const float*>(smem + CF::CC_GATE + stp * kGateBytes)[r64];
-      tc::fence_before_sync();
-      tc::mbar_arrive(&tempty[stp]);
-      return gr;
-    };
-    auto write_output = [&](int cp, float Gam_r) {
-      const int64_t t0p = t_beg + (int64_t)cp * kC;
-      const int nvp = (int)((L - (int64_t)cp * kC) < kC ? (L - (int64_t)cp * kC) : kC);
-      float o1[32], o2[32];
-      tc::tmem_ld16x2<32>(tmem + lane_base + TC_DO + DVS * (cp % 3), o1);
-      tc::tmem_ld16x2<32>(tmem + lane_base + TC_O2 + DVS * (cp % 3), o2);
-      if (r64 < nvp) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o1[i] = p.scale * fmaf(Gam_r, o1[i], o2[i]);
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((t0p + r64) * p.h_v + h) * (int64_t)p.d_v +
-                                              s * DVS + 32 * blk);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint4 q4;
-          q4.x = pack_bf16(o1[8 * c4 + 0], o1[8 * c4 + 1]);
-          q4.y = pack_bf16(o1[8 * c4 + 2], o1[8 * c4 + 3]);
-          q4.z = pack_bf16(o1[8 * c4 + 4], o1[8 * c4 + 5]);
-          q4.w = pack_bf16(o1[8 * c4 + 6], o1[8 * c4 + 7]);
-          dst[c4] = q4;
-        }
-      }
-    };
-    auto stage_state = [&](float (&sc)[32], int cn) {
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-        st_chunk<2>(smem + CF::CC_SS + b0 * 8192, jrow * 64 + c4 * 16, sc + 8 * c4);
-      const int stn = cn % NSTG;
-      ok = tc::mbar_wait(&tfull[stn], (cn / NSTG) & 1) && ok;
-      const float Gam_n =
-          reinterpret_cast<const float*>(smem + CF::CC_GATE + stn * kGateBytes)[128];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sc[i] *= Gam_n;
-      tc::tmem_st32(tmem + lane_base + TC_S + 32 * b0, sc);
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_ss);
-    };
-    // D_U of chunk cn accumulates onto U~ (so that U = U~ - W S^T comes out of
-    // the product itself); written by warps 0-3 right after they read D_U of
-    // the previous chunk, before they stage the state that the product waits for.
-    auto preload = [&](int cn) {
-      const int stn = cn % NSTG;
-      ok = tc::mbar_wait(&full[stn], (cn / NSTG) & 1) && ok;  // U~ arrived by bulk copy
-      const uint8_t* ut = smem + stn * CF::kMain + SC_U + blk * kPkgUSlice;  // row of U~, bf16
-      float u[32];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 q4 = *reinterpret_cast<const uint4*>(ut + tc::swizzle<2>(r64 * 64 + j * 16));
-        const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          u[8 * j + 2 * e] = __uint_as_float(w4[e] << 16);
-          u[8 * j + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-        }
-      }
-      tc::tmem_st16x2<32>(tmem + lane_base + TC_DU, u);
-    };
-    {  // initial state: rows 32 b0 .. of the slice, column jrow
-      float sc[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        sc[i] = p.state_in && jrow < DKP ? p.state_in[(srow0 + 32 * b0 + i) * DKP + jrow]
-                                         : 0.f;  // key columns past d_k stay zero
-      if (nchunks == 0) {
-        if (jrow < DKP)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p.state_out[(srow0 + 32 * b0 + i) * DKP + jrow] = sc[i];
-      } else {
-        if (warp < 4) preload(0);
-        stage_state(sc, 0);
-      }
-    }
-    float gam_prev = 0.f;  // output factor of the previous chunk's row (warps 4-7)
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % NSTG;
-      const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
-      if (warp < 4) {  // U = D_U: row r64, values 32 blk ..
-        ok = tc::mbar_wait(bar_d, c & 1) && ok;
-        tc::fence_after_sync();
-        const float dec_r = gates[64 + r64];
-        float u[32];
-        tc::tmem_ld16x2<32>(tmem + lane_base + TC_DU, u);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          st_chunk<2>(smem + CF::CC_UB + blk * 4096, r64 * 64 + c4 * 16, u + 8 * c4);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] *= dec_r;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          st_chunk<2>(smem + CF::CC_UK + blk * 4096, r64 * 64 + c4 * 16, u + 8 * c4);
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_u);
-        if (c + 1 < nchunks) preload(c + 1);  // D_U of chunk c has been read
-      } else {
-        if (c > 0) gam_prev = take_gates(c - 1);
-      }
-      ok = tc::mbar_wait(bar_s, c & 1) && ok;
-      tc::fence_after_sync();
-      float sc[32];
-      tc::tmem_ld32(tmem + lane_base + TC_S + 32 * b0, sc);
-      if (c == nchunks - 1) {
-        if (jrow < DKP)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p.state_out[(srow0 + 32 * b0 + i) * DKP + jrow] = sc[i];
-      } else {
-        stage_state(sc, c + 1);
-      }
-      if (warp >= 4 && c > 0) write_output(c - 1, gam_prev);  // after the staging
-    }
-    if (ok && nchunks > 0 && warp >= 4)  // the last output
-      write_output(nchunks - 1, take_gates(nchunks - 1));
-  }
-  if (!ok) raise_error(p.err, kErrDeviceTimeout);
-  tc::fence_before_sync();
-  tc::named_sync(kBarChainCta, CF::kThreads);
-  tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, 512);
-}
-
 // The chain of the two-kernel form: 32 state rows per CTA, 3 stages, 4
 // epilogue warps; or, when the batch's chains fill more than one wave of SMs,
 // 64 rows per CTA (N = 64 products, 8 epilogue warps), which costs less SM
@@ -1313,11 +1020,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     wait_prerequisites();  // the plan kernel's order
     n = p.order[blockIdx.x / (ns * p.h_v)];
   }
-  if constexpr (kRows == 64)
-    chain_run64<CF::kStages, DKP>(p, &tm_q, &tm_k, smem, n, h, s, threadIdx.x, nullptr);
-  else
-    chain_run<kRows, CF::kStages, CF::kEW, DKP>(p, &tm_q, &tm_k, smem, n, h, s, threadIdx.x,
-                                                nullptr);
+  chain_run<kRows, CF::kStages, CF::kEW, DKP>(p, &tm_q, &tm_k, smem, n, h, s, threadIdx.x,
+                                              nullptr);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1458,7 +1162,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     const int s = blockIdx.x % ns;
     const int h = (blockIdx.x / ns) % p.h_v;
     const int n = blockIdx.x / (ns * p.h_v);
-    chain_run64<CoopChain::kStages, DKP>(p, &tm_q, &tm_k, smem, n, h, s,
+    chain_run<kRows, CoopChain::kStages, CoopChain::kEW, DKP>(p, &tm_q, &tm_k, smem, n, h, s,
                                                          threadIdx.x, flags);
     return;
   }

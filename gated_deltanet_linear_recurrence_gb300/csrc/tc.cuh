@@ -173,18 +173,6 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// The matching store (shape 16x32bx2): thread t < 16 writes 32 consecutive
-// columns of lane (lane base) + t, thread t >= 16 the same lane at + kSplit.
-template <uint32_t kSplit>
-__device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const float (&v)[32]) {
-  uint32_t r[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
-  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, {%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};" ::"r"(taddr), "n"(kSplit), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-               : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // The same for 8 consecutive columns per lane.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
@@ -240,16 +228,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// True in lane 0 of the warp only: the lane that issues every tensor-core
-// instruction of an MMA warp.  It must be the same lane each time, because a
-// tcgen05.commit tracks only the MMAs its own thread issued: the kernels rely
-// on a commit also covering products issued earlier in other places (a later
-// barrier covering the reads of an earlier product).  elect.sync does not
-// promise the same leader from one call to the next; with it, outputs of the
-// chunked prefill were measured to differ by an ulp in a few elements from run
-// to run (an earlier product still read a buffer that a later commit's waiters
-// had already rewritten).
-__device__ __forceinline__ bool elect_one() { return (threadIdx.x & 31) == 0; }
+// True in exactly one lane of a converged warp (elect.sync).  An MMA warp
+// calls it once and keeps the result: that lane then issues every product and
+// every tcgen05.commit of the warp.  The leader is not promised to be the same
+// lane from one elect.sync to the next, and a commit tracks only the products
+// its own thread issued, while the kernels rely on a later commit covering
+// earlier products (a buffer is rewritten once a later barrier completes);
+// electing per block made outputs differ by an ulp from run to run.  (Issuing
+// from lane 0 by index measured ~6 % slower per prefill call, and committing
+// from all 32 lanes 2.3x slower.)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 r;\n\telect.sync r|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 // Arrive once on `bar` when every MMA this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
