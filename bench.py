@@ -40,29 +40,30 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "40b9cf8e161f5350",
-                    "bytes": (68_258_816 + 31_124_736) + (118_789_888 + 12_016_384),
+                    "sha256_16": "6de4fe00327e3fb7",
+                    "bytes": (68_273_664 + 31_427_328) + (118_813_696 + 12_037_376),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                   "sha256_16": "40b9cf8e161f5350", "bytes": 68_702_720 + 66_749_696,
+                   "sha256_16": "6de4fe00327e3fb7", "bytes": 68_594_944 + 67_793_408,
                    "profile": "profiles/chunk_coop_t4096.md"},
     "chunk_coop@prefill_t131072": {
         "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-        "sha256_16": "40b9cf8e161f5350", "bytes": 5_413_437_952 + 3_772_615_168,
+        "sha256_16": "6de4fe00327e3fb7", "bytes": 2_194_089_472 + 3_743_292_160,
         "profile": "profiles/chunk_coop_t131072.md"},
     "chunk_split@prefill_varlen10": {
         "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-        "sha256_16": "40b9cf8e161f5350",
-        "bytes": 12_800 + (4_363_545_088 + 5_380_021_248) + (7_594_119_168 + 2_140_511_488),
+        "sha256_16": "6de4fe00327e3fb7",
+        "bytes": 12_544 + (4_363_200_256 + 5_379_811_328) + (7_593_478_912 + 2_140_528_640),
         "profile": "profiles/chunk_split_varlen10.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                      "sha256_16": "1687ce9fb8434170", "bytes": 68_217_344 + 5_661_952,
+                      "sha256_16": "f95c4a11744de65c", "bytes": 68_218_112 + 5_280_768,
                       "profile": "profiles/chunk_prefill_t4096.md"},
     "attn_decode": {"files": ["attn_decode.cu", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "5f6befb361bfe092", "bytes": 268_506_368 + 2_978_048,
+                    "sha256_16": "485f911bcb6786c8",
+                    "bytes": (268_509_696 + 3_135_488) + 1_264_896,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
-                    "sha256_16": "6bc3ccc0013040f8", "bytes": 541_250_560 + 480_322_304,
+                    "sha256_16": "2f08de81c80328b4", "bytes": 541_150_464 + 480_271_360,
                     "profile": "profiles/decode_step_b256.md"},
 }
 
