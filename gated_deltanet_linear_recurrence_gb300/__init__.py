@@ -22,7 +22,7 @@ __all__ = ["gdn_prefill", "gdn_prefill_streamed", "gdn_prefill_streamed_workspac
            "gdn_prefill_form", "gdn_selftest_wait_timeout", "GdnError",
            "STATUS_NAMES", "NOALLOC_SCRATCH_BYTES"]
 
-NOALLOC_SCRATCH_BYTES = 96 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
+NOALLOC_SCRATCH_BYTES = 128 << 20  # GDN_NOALLOC_SCRATCH_BYTES in include/gdn.h
 
 _DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
 

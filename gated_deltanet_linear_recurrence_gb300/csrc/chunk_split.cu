@@ -60,9 +60,9 @@
 namespace gdn {
 
 // Workspace layout (shared with the host-side size computation).
-constexpr uint32_t kPkgW = 0, kPkgP = 16384, kPkgU = 24576, kPkgGates = 40960;
+constexpr uint32_t kPkgW = 0, kPkgP = 16384, kPkgU = 24576, kPkgDK = 40960, kPkgGates = 57344;
 constexpr uint32_t kPkgUSlice = 4096;  // U~ of one 32-wide slice of d_v
-constexpr uint32_t kPkgBytes = 41984;  // 41 KB, a multiple of 1024 (swizzle phase)
+constexpr uint32_t kPkgBytes = 58368;  // 57 KB, a multiple of 1024 (swizzle phase)
 
 size_t split_header_bytes(int32_t num_seqs) {
   // chunk_base [N+1] and the state passes' sequence order [N]
@@ -180,23 +180,47 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
       : "memory");
 }
+// shared -> global, in the issuing thread's bulk group
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(tc::smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The thread's committed bulk stores have read their shared memory ...
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... or have completed.
+__device__ __forceinline__ void bulk_wait_done() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ prepare
 constexpr int kPrepThreads = 128;  // 4 warps; 4 CTAs per SM (TMEM, registers, shared memory)
 constexpr uint32_t kBarAll = 1, kBarGateP = 2;
 constexpr float kFactorRange = 80.f;  // |gamma| bound for Gamma_r / Gamma_i (e^80 < 2^127)
 // Shared memory of the prepare kernel, reused as the item advances:
-//   [0, 32K)     per d_k half kb: [Q 8K][K 8K] (TMA); after G: Q1 holds the
-//                solve scratch, then T diag(b Gamma); after W: K holds V (TMA)
+//   [0, 32K)     per d_k half kb: [Q 8K][K 8K] (TMA).  After G: Q0 stages P for
+//                its bulk store, then holds V's first 64 columns (TMA); Q1 holds
+//                the solve scratch, then T diag(b Gamma).  After W: K0 and Q1
+//                stage the two halves of -W.  After U~: K1 and Q0 stage U~.
 //   [32K, 49K)   A, then T: fp32 [64][kLdM]; then T diag(b) (bf16) at its start
+//                and V's last 64 columns (TMA) 8K further on
 //   gates        Gamma[64], decay[64], the mask column factors |k_i|^-1 / Gamma_i [64],
 //                gamma[64], beta[64], the reciprocal L2 norms of the chunk's k rows
 //                and q rows (1 without the normalisation option), and a flag: the
 //                chunk's gamma range allows the factorised masks
 constexpr uint32_t PP_KQ = 0;
 constexpr uint32_t PP_Q1 = 16384;                  // solve scratch, then T diag(b Gamma)
-constexpr uint32_t PP_V = 8192;                    // V halves over K0 and K1 (stride 16K)
+constexpr uint32_t PP_Q0 = 0, PP_K0 = 8192, PP_K1 = 24576;
 constexpr uint32_t PP_MF = 32768;
 constexpr uint32_t PP_TA = PP_MF;                  // T diag(b), once T is in registers
+constexpr uint32_t PP_V1 = PP_MF + 8192;           // V's columns 64-127 (V's 0-63 at Q0)
+static_assert(PP_V1 + 8192 <= PP_MF + 64 * kLdM * 4, "V's second half inside the solve buffer");
 constexpr uint32_t PP_GATE = PP_MF + 64 * kLdM * 4;
 constexpr uint32_t PP_MISC = PP_GATE + 7 * 64 * 4 + 16;  // + the factorisation flag
 constexpr uint32_t kPrepSmem = PP_MISC + 64 + 1024;
@@ -271,7 +295,9 @@ __device__ __forceinline__ void prepare_loads(const SplitParams& p, const CUtens
 // mbarriers `bars` (Q/K landed, an MMA done, V landed; initialised with count 1)
 // that have seen k earlier items, and the named barriers bA (128 threads) and
 // bG (threads 0-63); prepare_loads has been issued for it.  Writes the item's
-// package; false if a wait expired.
+// package: the gates with plain stores, P, -W and U~ staged in shared memory
+// and written by bulk copies that thread 96 issues, and has seen complete when
+// the item returns; false if a wait expired.
 // The barrier ids are run-time values so that the cooperative form's four
 // slots run one copy of this code (instruction-cache footprint).
 __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtensorMap* tm_v,
@@ -430,7 +456,7 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
       if (pw < 2) {
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
-          st_chunk<3>(pkg + kPkgP, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
+          st_chunk<3>(smem + PP_Q0, r * 128 + (4 * half + c8) * 16, a + 8 * c8);
       } else {
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4)
@@ -438,9 +464,39 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
               make_float4(a[4 * e4], a[4 * e4 + 1], a[4 * e4 + 2], a[4 * e4 + 3]);
       }
     }
+    tc::fence_proxy_async();  // P's staging before its bulk store
     tc::fence_before_sync();
     tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
+    if (pw >= 2) {  // warps 2-3 have no part in the solve's first level
+      if (pt == 96) {
+        bulk_s2g(pkg + kPkgP, smem + PP_Q0, 8192);
+        bulk_commit();
+        bulk_wait_read();  // then V's first 64 columns over the staged P
+        tc::mbar_arrive_expect_tx(bar_v, 16384);
+        tc::tma_load_2d(smem + PP_Q0, tm_v, h * p.d_v, y, bar_v);
+      }
+      // The state update's decayed K, diag(decay_r / |k_r|) K, into the package
+      // as an image of K's two swizzled 64-column halves: a row's 16-byte pieces
+      // move within its 128 bytes only, so piece o of the image is piece o of K
+      // scaled by its row's factor; consecutive threads take consecutive pieces
+      // (coalesced stores, conflict-free loads).
+      const int u = pt - 64;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t o = (uint32_t)(u + 64 * i) * 16;  // byte offset in the 16 KB image
+        const uint32_t kb = o >> 13, ob = o & 8191;
+        const float f = dec[ob >> 7] * rk[ob >> 7];
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + PP_KQ + kb * 16384 + 8192 + ob);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o4[e] = pack_bf16(__uint_as_float(w4[e] << 16) * f,
+                            __uint_as_float(w4[e] & 0xffff0000u) * f);
+        *reinterpret_cast<uint4*>(pkg + kPkgDK + o) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
 
     unit_lower_inverse<kPrepThreads>(MF, YF, pt, lane, bA);
 
@@ -485,6 +541,10 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     tc::fence_before_sync();
     tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
+    // V's columns 64-127 over the part of MF past T diag(b); columns past this
+    // head's d_v (d_v < 128) belong to the next head or lie outside the tensor
+    // (zero fill), and the slices built from them are never written
+    if (pt == 96) tc::tma_load_2d(smem + PP_V1, tm_v, h * p.d_v + 64, y, bar_v);
     if (pt == 64) {  // W = (T b Gamma) K: M=64 N=128 K=64 (over G's columns)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
@@ -498,18 +558,9 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
     ok = tc::named_sync_and(bA, kPrepThreads, ok);
   }
   if (ok) {
-    if (pt == 0) {  // K is consumed: V (two 64-column boxes) over K0 and K1
-      tc::mbar_arrive_expect_tx(bar_v, 16384);
-      // columns past this head's d_v (d_v < 128) belong to the next head or
-      // lie outside the tensor (zero fill); the slices built from them are
-      // never written
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-        tc::tma_load_2d(smem + PP_V + kb * 16384, tm_v, h * p.d_v + 64 * kb, y, bar_v);
-    }
-    // -W (M=64 accumulator: row 16 w + l on lanes l = 0-15 of warp w's quarter) to
-    // the package; thread l < 16 takes columns 32 q .., thread l + 16 the same row's
-    // columns 64 + 32 q ..
+    // -W (M=64 accumulator: row 16 w + l on lanes l = 0-15 of warp w's quarter),
+    // staged in K0 (columns 0-63) and Q1 (64-127); thread l < 16 takes columns
+    // 32 q .., thread l + 16 the same row's columns 64 + 32 q ..
     const int r = 16 * pw + (lane & 15), hi = lane >> 4;
     float w[32];
 #pragma unroll 1
@@ -519,24 +570,32 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
       for (int e = 0; e < 32; ++e) w[e] = -w[e];
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8)
-        st_chunk<3>(pkg + kPkgW + hi * 8192, r * 128 + (4 * q + c8) * 16, w + 8 * c8);
+        st_chunk<3>(smem + (hi ? PP_Q1 : PP_K0), r * 128 + (4 * q + c8) * 16, w + 8 * c8);
     }
+    tc::fence_proxy_async();
     tc::fence_before_sync();
     tc::named_sync(bA, kPrepThreads);  // W's columns are read before U~ overwrites them
     tc::fence_after_sync();
+    if (pt == 96) {
+      bulk_s2g(pkg + kPkgW, smem + PP_K0, 8192);
+      bulk_s2g(pkg + kPkgW + 8192, smem + PP_Q1, 8192);
+      bulk_commit();
+    }
     if (pt == 64 && tc::mbar_wait(bar_v, k & 1)) {  // (on a timeout nothing commits: all time out)
       tc::fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // U~ = (T b) V: M=64 N=128 K=64
         tc::mma_bf16(tmem, tc::smem_desc(sbase + PP_TA + kk * 32, 16, 1024, tc::kLayoutSw128),
-                     tc::smem_desc(sbase + PP_V + kk * 2048, 16384, 1024, tc::kLayoutSw128), IDP_W,
+                     tc::smem_desc(sbase + PP_Q0 + kk * 2048, PP_V1 - PP_Q0, 1024,
+                                   tc::kLayoutSw128),
+                     IDP_W,
                      kk > 0);
       tc::mma_commit(bar_mma);
     }
     ok = tc::mbar_wait(bar_mma, (3 * k + 2) & 1);
     tc::fence_after_sync();
     ok = tc::named_sync_and(bA, kPrepThreads, ok);
-    if (ok) {  // U~ slices (bf16, 64-byte rows with the SW64 XOR pattern) to the package
+    if (ok) {  // U~ slices (bf16, 64-byte rows with the SW64 XOR pattern): 0-1 in K1, 2-3 in Q0
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {
         tc::tmem_ld16x2<64>(tmem + lane_base + 32 * q, w);
@@ -544,10 +603,27 @@ __device__ __forceinline__ bool prepare_item(const SplitParams& p, const CUtenso
         if (sl * kDVS < p.d_v) {
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8)
-            st_chunk<2>(pkg + kPkgU + sl * kPkgUSlice, r * 64 + c8 * 16, w + 8 * c8);
+            st_chunk<2>(smem + (hi ? PP_Q0 : PP_K1) + q * kPkgUSlice, r * 64 + c8 * 16,
+                        w + 8 * c8);
         }
       }
     }
+  }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  tc::named_sync(bA, kPrepThreads);
+  tc::fence_after_sync();
+  if (pt == 96) {  // U~'s bulk stores; every store of the item complete before it returns
+    if (ok) {
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl)
+        if (sl * kDVS < p.d_v)
+          bulk_s2g(pkg + kPkgU + sl * kPkgUSlice,
+                   smem + ((sl >> 1) ? PP_Q0 : PP_K1) + (sl & 1) * kPkgUSlice, kPkgUSlice);
+      bulk_commit();
+    }
+    bulk_wait_done();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   return ok;
 }
@@ -621,15 +697,17 @@ struct ChainCfg {
   static constexpr uint32_t kMainTx = 4 * 8192 + 2 * 8192 + NB * kPkgUSlice;
   static constexpr uint32_t CC_TAIL = NSTG * kMain;
   static constexpr uint32_t CC_SS = CC_TAIL + NSTG * kTail;  // S^T bf16 [j][i]: NB x [128][32]
-  static constexpr uint32_t CC_UB = CC_SS + NB * 8192;       // U bf16 [r][i]: NB x [64][32]
-  static constexpr uint32_t CC_UK = CC_UB + NB * 4096;       // decayed U, same layout
-  static constexpr uint32_t CC_GATE = CC_UK + NB * 4096;    // NSTG x kGateBytes
+  // U bf16 [r][i]: NB x [64][32], two buffers (chunk parity), so that U of a
+  // chunk is staged while P U of the previous one may still be reading its own
+  static constexpr uint32_t CC_UB = CC_SS + NB * 8192;
+  static constexpr uint32_t kUB = NB * 4096;
+  static constexpr uint32_t CC_GATE = CC_UB + 2 * kUB;       // NSTG x kGateBytes
   static constexpr uint32_t CC_MISC = CC_GATE + NSTG * kGateBytes;
   static constexpr uint32_t kSmem = CC_MISC + 256 + 1024;
   static constexpr uint32_t kTmemCols = DVS == 32 ? 256 : 512;
   static constexpr uint32_t TC_D0 = 0, TC_O0 = 3 * DVS, TC_S = 6 * DVS;  // D, P U triple-buffered
   static constexpr uint32_t IDC_WQ = tc::idesc_bf16_f32(128, DVS, false, true);  // [-W; Q] S^T
-  static constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, DVS, true, true);   // K^T (decay U)
+  static constexpr uint32_t IDC_SU = tc::idesc_bf16_f32(128, DVS, true, true);   // (decay K)^T U
   static constexpr uint32_t IDC_PU = tc::idesc_bf16_f32(128, DVS, false, true);  // [.; P] U
   static_assert(DVS == 32 || DVS == 64, "32 or 64 state rows per CTA");
   static_assert((EW == 4 || EW == 8) && BPW >= 1, "4 or 8 epilogue warps, at most one per block");
@@ -746,7 +824,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           kq_load<DKP>(dst + kb * kHalf + SC_Q, tm_q, hk, kb, y, fb);
-          kq_load<DKP>(dst + kb * kHalf + SC_K, tm_k, hk, kb, y, fb);
+          bulk_g2s(dst + kb * kHalf + SC_K, pkg + kPkgDK + kb * 8192, 8192, fb);
           bulk_g2s(dst + kb * kHalf + SC_W, pkg + kPkgW + kb * 8192, 8192, fb);
         }
         bulk_g2s(dst + SC_U, pkg + kPkgU + s * CF::NB * kPkgUSlice, CF::NB * kPkgUSlice, fb);
@@ -773,7 +851,6 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     // offset / 16 to the start-address field (every address is below 256 KB).
     // The leading byte offset steps between the 32-value blocks (DVS = 64).
     const uint64_t dSS = tc::smem_desc(sbase + CF::CC_SS, 8192, 512, tc::kLayoutSw64);
-    const uint64_t dUK = tc::smem_desc(sbase + CF::CC_UK, 4096, 512, tc::kLayoutSw64);
     const uint64_t dUB = tc::smem_desc(sbase + CF::CC_UB, 4096, 512, tc::kLayoutSw64);
     const uint64_t dW0 = tc::smem_desc(sbase + SC_W, 16, 1024, tc::kLayoutSw128);
     const uint64_t dK0 = tc::smem_desc(sbase + SC_K, kHalf, 1024, tc::kLayoutSw128);
@@ -784,6 +861,7 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       const int st = c % NSTG;
       const uint64_t so = (uint64_t)((st * CF::kMain) >> 4), to = (uint64_t)((st * kTail) >> 4);
       const uint64_t dW = dW0 + so, dK = dK0 + so, dP = dP0 + to;
+      const uint64_t dU = dUB + (uint64_t)(((c & 1) * CF::kUB) >> 4);
       const uint32_t td = tmem + CF::TC_D0 + DVS * (c % 3), to2 = tmem + CF::TC_O0 + DVS * (c % 3);
       if (!(ok = warp_wait(&full[st], (c / NSTG) & 1) && warp_wait(bar_ss, c & 1))) break;
       if (leader) {
@@ -798,8 +876,8 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       if (!(ok = warp_wait(bar_u, c & 1))) break;
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // S^T += K^T (decayed U), onto Gamma_n S^T
-          tc::mma_bf16(tmem + CF::TC_S, dK + ((kk * 2048) >> 4), dUK + ((kk * 1024) >> 4),
+        for (int kk = 0; kk < 4; ++kk)  // S^T += (decayed K)^T U, onto Gamma_n S^T
+          tc::mma_bf16(tmem + CF::TC_S, dK + ((kk * 2048) >> 4), dU + ((kk * 1024) >> 4),
                        CF::IDC_SU, 1);
         tc::mma_commit(bar_s);
         tc::mma_commit(&empty[st]);  // the update has read K of the stage
@@ -809,17 +887,18 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // O2 = P U (rows 64-127)
-          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dUB + ((kk * 1024) >> 4), CF::IDC_PU, kk > 0);
+          tc::mma_bf16(to2, dP + ((kk * 32) >> 4), dU + ((kk * 1024) >> 4), CF::IDC_PU, kk > 0);
         tc::mma_commit(&bar_o[c % 3]);
       }
       __syncwarp();
     }
   } else if (warp < EW) {
-    // Epilogue warps.  Those on TMEM lanes 0-63 form U and preload the next
-    // chunk's U~; those on lanes 64-127 take the previous chunk's gates, clear
-    // rows 64-127 of the next D buffer and, once the state is staged, store the
-    // previous chunk's output; all stage the state.  Every hand-off is an
-    // mbarrier with a bounded wait.
+    // Epilogue warps.  Those on TMEM lanes 0-63 form U (staged once: the update
+    // takes the package's decayed K, so no per-row scaling is left on this
+    // critical step) and preload the next chunk's U~; those on lanes 64-127
+    // take the previous chunk's gates, clear rows 64-127 of the next D buffer
+    // and, once the state is staged, store the previous chunk's output; all
+    // stage the state.  Every hand-off is an mbarrier with a bounded wait.
     const int rl = 32 * (warp & 1) + lane;  // accumulator row of this thread within its half
     // Output of chunk cp (the warps on lanes 64-127): O = Gamma Q S^T + P U, in
     // two parts.  take_gates(cp) waits for P U, reads the rows' output factors
@@ -939,26 +1018,19 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     }
     float gam_prev = 0.f;  // output factor of the previous chunk's rows (output warps)
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % NSTG;
-      const float* gates = reinterpret_cast<const float*>(smem + CF::CC_GATE + st * kGateBytes);
       if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
         ok = tc::mbar_wait(bar_d, c & 1) && ok;
-        if (c > 0)  // P U of the previous chunk has read the U buffers about to be rewritten
-          ok = tc::mbar_wait(&bar_o[(c - 1) % 3], ((c - 1) / 3) & 1) && ok;
+        if (c > 1)  // P U of chunk c - 2 has read the U buffer about to be rewritten
+          ok = tc::mbar_wait(&bar_o[(c - 2) % 3], ((c - 2) / 3) & 1) && ok;
         tc::fence_after_sync();
-        const float dec_r = gates[64 + rl];
 #pragma unroll
         for (int b = b0; b < b0 + BPW; ++b) {
           float u[32];
           tc::tmem_ld32(tmem + lane_base + CF::TC_D0 + DVS * (c % 3) + 32 * b, u);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
-            st_chunk<2>(smem + CF::CC_UB + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] *= dec_r;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            st_chunk<2>(smem + CF::CC_UK + b * 4096, rl * 64 + c4 * 16, u + 8 * c4);
+            st_chunk<2>(smem + CF::CC_UB + (c & 1) * CF::kUB + b * 4096, rl * 64 + c4 * 16,
+                        u + 8 * c4);
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -1136,7 +1208,7 @@ __device__ __forceinline__ void coop_prepare_slot(const SplitParams& p, const CU
     tc::fence_before_sync();
     tc::named_sync(bA, kPrepThreads);
     tc::fence_after_sync();
-    if (pt == 0 && ok)
+    if (pt == 96 && ok)  // the thread that saw the package's bulk stores complete
       asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flags + item), "r"(1) : "memory");
   }
   if (!ok && pt == 0) raise_error(p.err, kErrDeviceTimeout);

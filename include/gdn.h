@@ -160,7 +160,7 @@ gdn_status gdn_prefill_ex(const void* q, const void* k, const void* v, const flo
 /* Bytes of workspace for the fastest gdn_prefill path with these arguments
  * (0 when that path uses none); for GDN_ALGO_CHUNKED_SPLIT and
  * GDN_ALGO_CHUNKED_COOP, the bytes each needs.  An upper bound computed from the
- * host arguments: the 1 KB-rounded (N+1) int32 header + I * 41 KB with
+ * host arguments: the 1 KB-rounded (2N+1) int32 header + I * 57 KB with
  * I = (T/64 + N + 1) * h_v items, plus (I + 1) int32 ready flags (1 KB-rounded)
  * except for GDN_ALGO_CHUNKED_SPLIT. */
 size_t gdn_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_k,
@@ -249,8 +249,8 @@ size_t gdn_prefill_host_workspace_size(int64_t piece_tokens, int32_t h_k, int32_
  * a multiple of 32 (else GDN_ERR_UNSUPPORTED_*).  Limit: returns
  * GDN_ERR_WORKSPACE_TOO_SMALL, touching no device, when
  * gdn_prefill_workspace_size(..., GDN_ALGO_CHUNKED_SPLIT) for these arguments
- * exceeds GDN_NOALLOC_SCRATCH_BYTES (96 MiB: e.g. one 4,096-token sequence at
- * 32 value heads needs 88.7 MB); larger problems go through gdn_prefill with a
+ * exceeds GDN_NOALLOC_SCRATCH_BYTES (128 MiB: e.g. one 4,096-token sequence at
+ * 32 value heads needs 123.3 MB); larger problems go through gdn_prefill with a
  * workspace.
  *
  * Set-up: the first call with a given device current looks up that device's
@@ -266,7 +266,7 @@ size_t gdn_prefill_host_workspace_size(int64_t piece_tokens, int32_t h_k, int32_
  * threads) race on it: order them, e.g. on one stream.  The array takes
  * GDN_NOALLOC_SCRATCH_BYTES of each device where the library's code is loaded.
  */
-#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)96 << 20)
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
 
 gdn_status gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g,
                                const float* beta, const float* state_in, float* state_out,

@@ -93,8 +93,8 @@ def test_noalloc_host_errors(lib):
         return lib.gdn_prefill_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, n, t,
                                        h_k, h_v, d_k, d_v, dtype, 1.0, None)
     big = 1 << 20   # 1M tokens at 2 value heads: ~1.1 GB of scratch
-    assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 96 << 20
-    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 96 << 20
+    assert lib.gdn_prefill_workspace_size(1, big, 1, 2, 128, 32, 1, 4) > 128 << 20
+    assert lib.gdn_prefill_workspace_size(1, 4096, 16, 32, 128, 128, 1, 4) <= 128 << 20
     assert call(t=big) == 7                              # GDN_ERR_WORKSPACE_TOO_SMALL
     assert call(d_k=32) == 3                             # chunked needs d_k 64 or 128
     assert call(dtype=0) == 4                            # and bf16
@@ -131,9 +131,9 @@ def test_workspace_and_crossover_queries(lib):
     # four prompts at 32 value heads: the table takes the two kernels from any length
     assert ws(4, 1000, 0) == ws(4, 1000, 5) > 0
     assert ws(4, 2048, 2) == ws(4, 2048, 5) > ws(4, 2048, 4) > 0
-    # header (1 KB-rounded) + I = (T/64 + N + 1) x h_v per-chunk packages of 41 KB
+    # header (1 KB-rounded) + I = (T/64 + N + 1) x h_v per-chunk packages of 57 KB
     items = (2048 // 64 + 5) * 32
-    assert ws(4, 2048, 4) == 1024 + items * 41984
+    assert ws(4, 2048, 4) == 1024 + items * 58368
     # the cooperative form adds one ready flag per item and a counter, 1 KB-rounded
     assert ws(4, 2048, 5) == ws(4, 2048, 4) + ((items + 1) * 4 + 1023) // 1024 * 1024
     x = lib.gdn_prefill_crossover_tokens(16, 32, 128, 128, 1)
