@@ -1019,9 +1019,11 @@ __device__ __forceinline__ void chain_run(const SplitParams& p, const CUtensorMa
     float gam_prev = 0.f;  // output factor of the previous chunk's rows (output warps)
     for (int c = 0; c < nchunks && ok; ++c) {
       if ((warp & 3) < 2) {  // U = U~ - W S^T for rows r = lanes 0-63
+        // D(c) completes after P U(c - 2), the last reader of the U buffer about
+        // to be rewritten: one thread issued both and committed bar_d after D(c),
+        // and a commit covers every earlier product of its thread.  (Waiting on
+        // P U(c - 2)'s own barrier here measured ~2 % slower per call.)
         ok = tc::mbar_wait(bar_d, c & 1) && ok;
-        if (c > 1)  // P U of chunk c - 2 has read the U buffer about to be rewritten
-          ok = tc::mbar_wait(&bar_o[(c - 2) % 3], ((c - 2) / 3) & 1) && ok;
         tc::fence_after_sync();
 #pragma unroll
         for (int b = b0; b < b0 + BPW; ++b) {
