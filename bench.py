@@ -40,20 +40,20 @@ FP32_LANES_PER_SM = 128
 # stripped) hash to the recorded value.
 NCU_TRAFFIC = {
     "chunk_split": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                    "sha256_16": "6de4fe00327e3fb7",
-                    "bytes": (68_273_664 + 31_427_328) + (118_813_696 + 12_037_376),
+                    "sha256_16": "4dbd7899e795fe3c",
+                    "bytes": (68_258_048 + 62_212_608) + (135_572_224 + 13_334_784),
                     "profile": "profiles/chunk_split_t4096.md"},
     "chunk_coop": {"files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-                   "sha256_16": "6de4fe00327e3fb7", "bytes": 68_594_944 + 67_793_408,
+                   "sha256_16": "4dbd7899e795fe3c", "bytes": 69_837_312 + 99_008_000,
                    "profile": "profiles/chunk_coop_t4096.md"},
     "chunk_coop@prefill_t131072": {
         "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-        "sha256_16": "6de4fe00327e3fb7", "bytes": 2_194_089_472 + 3_743_292_160,
+        "sha256_16": "4dbd7899e795fe3c", "bytes": 4_049_355_008 + 4_838_642_176,
         "profile": "profiles/chunk_coop_t131072.md"},
     "chunk_split@prefill_varlen10": {
         "files": ["chunk_split.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
-        "sha256_16": "6de4fe00327e3fb7",
-        "bytes": 12_544 + (4_363_200_256 + 5_379_811_328) + (7_593_478_912 + 2_140_528_640),
+        "sha256_16": "4dbd7899e795fe3c",
+        "bytes": 12_544 + (4_362_177_024 + 7_522_012_928) + (8_666_622_720 + 2_143_017_984),
         "profile": "profiles/chunk_split_varlen10.md"},
     "chunk_prefill": {"files": ["chunk_prefill.cu", "chunk_common.cuh", "tc.cuh", "rows.cuh"],
                       "sha256_16": "f95c4a11744de65c", "bytes": 68_218_112 + 5_280_768,
