@@ -69,40 +69,40 @@ struct CrossoverEntry {
 constexpr int64_t kNever = INT64_MAX;
 constexpr CrossoverEntry kCrossover[] = {
     // d_k, d_v, h_v, N: {scan below, two kernels from, cooperative from}
-    {128, 128, 32, 1, {16, 256, 4096}},
+    {128, 128, 32, 1, {8, 256, 4096}},
     {128, 128, 32, 4, {16, 8, kNever}},
     {128, 128, 32, 16, {8, 8, kNever}},
-    {128, 128, 4, 1, {16, 512, kNever}},
+    {128, 128, 4, 1, {16, 256, kNever}},
     {128, 128, 4, 4, {16, 512, kNever}},
-    {128, 128, 4, 16, {16, 128, kNever}},
-    {128, 64, 32, 1, {16, 256, 8192}},
-    {128, 64, 32, 4, {32, 128, kNever}},
+    {128, 128, 4, 16, {32, 128, kNever}},
+    {128, 64, 32, 1, {16, 256, 4096}},
+    {128, 64, 32, 4, {16, 128, kNever}},
     {128, 64, 32, 16, {16, 8, kNever}},
     {128, 64, 4, 1, {16, 256, kNever}},
-    {128, 64, 4, 4, {8, 512, kNever}},
+    {128, 64, 4, 4, {8, 256, kNever}},
     {128, 64, 4, 16, {16, 512, kNever}},
     {128, 32, 32, 1, {16, 256, kNever}},
-    {128, 32, 32, 4, {16, 1024, kNever}},
-    {128, 32, 32, 16, {32, 256, kNever}},
+    {128, 32, 32, 4, {16, 4096, kNever}},
+    {128, 32, 32, 16, {32, 1024, kNever}},
     {128, 32, 4, 1, {16, 256, kNever}},
     {128, 32, 4, 4, {16, 512, kNever}},
     {128, 32, 4, 16, {16, 512, kNever}},
     {64, 128, 32, 1, {16, 0, 4096}},
     {64, 128, 32, 4, {32, 0, kNever}},
     {64, 128, 32, 16, {16, 0, kNever}},
-    {64, 128, 4, 1, {32, 0, kNever}},
+    {64, 128, 4, 1, {16, 0, kNever}},
     {64, 128, 4, 4, {32, 0, kNever}},
     {64, 128, 4, 16, {32, 0, kNever}},
-    {64, 64, 32, 1, {16, 0, 8192}},
+    {64, 64, 32, 1, {16, 0, 4096}},
     {64, 64, 32, 4, {32, 0, kNever}},
     {64, 64, 32, 16, {32, 0, kNever}},
     {64, 64, 4, 1, {16, 0, kNever}},
     {64, 64, 4, 4, {32, 0, kNever}},
     {64, 64, 4, 16, {32, 0, kNever}},
-    {64, 32, 32, 1, {32, 0, kNever}},
+    {64, 32, 32, 1, {16, 0, kNever}},
     {64, 32, 32, 4, {32, 0, kNever}},
     {64, 32, 32, 16, {64, 0, kNever}},
-    {64, 32, 4, 1, {32, 0, kNever}},
+    {64, 32, 4, 1, {16, 0, kNever}},
     {64, 32, 4, 4, {32, 0, kNever}},
     {64, 32, 4, 16, {32, 0, kNever}},
 };
