@@ -63,7 +63,7 @@ NCU_TRAFFIC = {
                     "bytes": (268_509_696 + 3_135_488) + 1_264_896,
                     "profile": "profiles/attn_decode_b1_l131072.md"},
     "decode_step": {"files": ["decode_step.cu", "rows.cuh", "tc.cuh"],
-                    "sha256_16": "2f08de81c80328b4", "bytes": 541_150_464 + 480_271_360,
+                    "sha256_16": "52eb19cd391aa574", "bytes": 541_265_152 + 480_637_184,
                     "profile": "profiles/decode_step_b256.md"},
 }
 

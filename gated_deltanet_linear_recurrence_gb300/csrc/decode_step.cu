@@ -24,7 +24,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kDecodeWarps = 4;
+constexpr int kDecodeWarps = 4;  // warps per CTA of the large-batch and normalising steps
 
 // The step for the warp's rows row0 ..: loads, update and in-place store of the
 // state rows; returns this lane's output value, and whether the lane holds one
@@ -117,8 +117,8 @@ struct OutNorm {
   float eps;
 };
 
-template <int DK, int R, bool kPrefetch, bool kNorm, typename T>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+template <int DK, int R, int W, bool kPrefetch, bool kNorm, typename T>
+__global__ void __launch_bounds__(W * 32)
     decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const float* __restrict__ g, const float* __restrict__ beta,
                        float* __restrict__ state, T* __restrict__ o, int32_t h_k, int32_t h_v,
@@ -131,10 +131,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int b = blockIdx.x / blocks_per_head;
   const int rb = blockIdx.x - b * blocks_per_head;
   const int h = blockIdx.y;
-  const int row0 = (rb * kDecodeWarps + warp) * LY::kRowsPerWarp;
+  const int row0 = (rb * W + warp) * LY::kRowsPerWarp;
   if constexpr (kNorm) {
     // every warp takes part in the cluster's reduction, idle ones with nothing
-    __shared__ float part[kDecodeWarps + 1];
+    __shared__ float part[W + 1];
     float sq = 0.f, out = 0.f;
     int row_mine = 0;
     bool mine = false;
@@ -149,13 +149,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (threadIdx.x == 0) {
       float t = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) t += part[w];
-      part[kDecodeWarps] = t;
+      for (int w = 0; w < W; ++w) t += part[w];
+      part[W] = t;
     }
     tc::cluster_sync();  // every CTA's partial sum is written
     if (threadIdx.x == 0) {
       float t = 0.f;
-      for (int r = 0; r < blocks_per_head; ++r) t += tc::ld_cluster_f32(&part[kDecodeWarps], r);
+      for (int r = 0; r < blocks_per_head; ++r) t += tc::ld_cluster_f32(&part[W], r);
       part[0] = rsqrtf(t / (float)d_v + nrm.eps);  // own slot 0 is read by no other CTA
     }
     tc::cluster_sync();  // the partial sums have been read: no CTA leaves before that
@@ -173,10 +173,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
 }
 
-template <int DK, int R, bool kPrefetch, bool kNorm, typename T>
+template <int DK, int R, int W, bool kPrefetch, bool kNorm, typename T>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int L = DK / 4;
-  constexpr int rows_per_block = kDecodeWarps * RowLayout<DK, L, R>::kRowsPerWarp;
+  constexpr int rows_per_block = W * RowLayout<DK, L, R>::kRowsPerWarp;
   const int blocks_per_head = (a.d_v + rows_per_block - 1) / rows_per_block;
   const int64_t gx = (int64_t)a.batch * blocks_per_head;
   if (gx > 0x7fffffffLL || a.h_v > 65535) return cudaErrorInvalidConfiguration;
@@ -190,11 +190,11 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
   if (kNorm && blocks_per_head > 8) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx, (unsigned)a.h_v);
-  cfg.blockDim = dim3(kDecodeWarps * 32);
+  cfg.blockDim = dim3(W * 32);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = kNorm ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_step_kernel<DK, R, kPrefetch, kNorm, T>,
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<DK, R, W, kPrefetch, kNorm, T>,
                             static_cast<const T*>(a.q), static_cast<const T*>(a.k),
                             static_cast<const T*>(a.v), a.g, a.beta, a.state, static_cast<T*>(a.o),
                             a.h_k, a.h_v, a.d_v, blocks_per_head, a.scale, a.qk_norm,
@@ -202,24 +202,30 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 // Rows per lane group: R = L/2 gives 16 rows per warp (most bytes in flight
-// per warp); with few rows in total a smaller R spreads the work over more SMs,
-// and the state is prefetched into L2 ahead of the dependency wait (measured
-// on GB300, batch 1 through 30 layers in one CUDA graph: 78.3 -> 70.1 us per
-// step; 8 rows per warp instead of 4 measured 86.5 us).  With the output
-// normalisation a head's CTAs (at most 8) form one cluster.
+// per warp) in CTAs of four warps.  With few rows in total the state is
+// prefetched into L2 ahead of the dependency wait, and the CTAs are single
+// warps of L/4 x (32/L) rows (8 rows at d_k = 128), so that more SMs stream at
+// once and the next call's CTAs find room early.  Measured on GB300, batch 1
+// through 30 layers in one CUDA graph (us per step): 78.3 without the prefetch
+// in four-warp CTAs of 4 rows per warp, 70.1 with it; then with the prefetch,
+// by warps per CTA x rows per warp: 8 x 4 78.3, 4 x 4 69.1, 2 x 4 66.0, 1 x 4
+// 59.9, 1 x 8 57.8, 1 x 1 145.9, and 1 x 4 without the prefetch 68.1.  With
+// the output normalisation a head's CTAs (at most 8) form one cluster, so that
+// step keeps four-warp CTAs.
 template <int DK, typename T>
 cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int L = DK / 4;
   constexpr int R_BIG = L / 2;
-  constexpr int R_SMALL = (L / 8) > 0 ? (L / 8) : 1;
+  constexpr int R_SMALL = (L / 8) > 0 ? (L / 8) : 1;   // normalising step, four warps
+  constexpr int R_ONE = (L / 4) > 0 ? (L / 4) : 1;     // single-warp CTAs
   const int64_t rows = (int64_t)a.batch * a.h_v * a.d_v;
   // 16 rows per warp still gives >= 4 warps on every one of 152 SMs
   const bool big = rows >= (int64_t)16 * 4 * 152 * kDecodeWarps;
   if (a.out_norm)
-    return big ? launch_t<DK, R_BIG, false, true, T>(a, stream)
-               : launch_t<DK, R_SMALL, true, true, T>(a, stream);
-  return big ? launch_t<DK, R_BIG, false, false, T>(a, stream)
-             : launch_t<DK, R_SMALL, true, false, T>(a, stream);
+    return big ? launch_t<DK, R_BIG, kDecodeWarps, false, true, T>(a, stream)
+               : launch_t<DK, R_SMALL, kDecodeWarps, true, true, T>(a, stream);
+  return big ? launch_t<DK, R_BIG, kDecodeWarps, false, false, T>(a, stream)
+             : launch_t<DK, R_ONE, 1, true, false, T>(a, stream);
 }
 
 template <typename T>
